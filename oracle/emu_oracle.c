@@ -1,0 +1,424 @@
+/*
+ * emu_oracle.c -- plain CPU oracle for FP32 GEMM emulated with BF16x9 and TF32x3.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call this file:
+ * only the tests, the smoke check and the CPU-baseline leg of the benchmark do.
+ * It shares no code, header, table or helper with the CUDA library.
+ *
+ * Sources (cited by title and section):
+ *   [Blog] "Unlocking Tensor Core performance for machine-learning interatomic
+ *          potentials" (NVIDIA technical blog), sections
+ *          "How Tensor Core FP32 bridges the hardware gap" (Fig. 1, Fig. 2, Eq. 1),
+ *          "TF32x3 on Ampere GPUs", "Limitations and decision criteria".
+ *
+ * What is computed, step by step, in the order the blog describes it:
+ *   1. split each FP32 operand into low-precision components
+ *        BF16x9: three scaled BF16 components            ([Blog] Fig. 1)
+ *        TF32x3: a leading and a residual TF32 component  ([Blog] Fig. 2)
+ *   2. form the selected cross products of components (exact in FP32)
+ *   3. accumulate them in FP32
+ *        BF16x9: along the five anti-diagonal bands i+j = 0..4, then recombine
+ *                with the scale factors                    ([Blog] Fig. 1)
+ *        TF32x3: hi*hi + hi*lo + lo*hi, lo*lo dropped       ([Blog] Eq. 1)
+ * and the plain definitions the method is judged against:
+ *   - the float64 GEMM (products and sums in binary64, sequential in k);
+ *   - the native FP32 SGEMM (sequential round-to-nearest fmaf over k), the
+ *     "native FP32" accuracy the blog compares against
+ *     ([Blog] "Limitations and decision criteria").
+ *
+ * Readings where the blog is silent (each is listed with its reason in the
+ * design notes of the repository):
+ *   - BF16x9 scale: 2^8 per component level; 8 is the BF16 significand width,
+ *     so the three components cover the 24-bit FP32 significand exactly.
+ *   - BF16x9 rounding of each component: toward zero (keep the top 16 bits of
+ *     the FP32 word).  The split is then exact for every finite FP32 value.
+ *   - TF32x3 rounding: hi = nearest TF32 (ties to even), lo = nearest TF32 of
+ *     the exact residual a - hi.  A second variant takes hi by truncation
+ *     (TF32X3_HI_RZ), which is what a tensor core does when it ignores the
+ *     low 13 bits of an FP32 container.
+ *   - Band accumulation: one FP32 round-to-nearest sum per band, sequential in
+ *     k, adding the band's products in (i, j) order with i ascending; then
+ *     recombination smallest band first.  A second variant keeps one FP32 sum
+ *     and adds, for each k, bands 4 down to 0 into it.
+ *   - alpha/beta/bias: C = fmaf(alpha, acc, beta * C_old) + bias; beta == 0
+ *     never reads C_old.
+ *
+ * Matrices are row-major.  op(A) is M x K: A[m*lda + k] when transA == 0,
+ * A[k*lda + m] when transA == 1.  op(B) is K x N: B[k*ldb + n] when
+ * transB == 0, B[n*ldb + k] when transB == 1.  C is M x N with leading
+ * dimension ldc.  The row list `rows` (NULL = all rows) lets a caller
+ * evaluate a sample of the output rows of a large problem.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fPIC -shared [-fopenmp].  Contraction
+ * must stay off: every multiply and add below is meant to round separately,
+ * and fmaf is written where a fused operation is meant.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+
+#define ORACLE_API __attribute__((visibility("default")))
+
+/* ------------------------------------------------------------------------ */
+/* bit helpers                                                              */
+/* ------------------------------------------------------------------------ */
+static inline uint32_t bits_of(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+static inline float float_of(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+
+/* Round toward zero to BF16: keep sign, exponent and the top 7 fraction bits. */
+static inline float bf16_rz(float x) { return float_of(bits_of(x) & 0xFFFF0000u); }
+
+/* Round to nearest, ties to even, to TF32 (10 fraction bits).  Inf and NaN
+ * pass through unchanged; a finite value beyond the largest TF32 number
+ * rounds to infinity, as IEEE rounding to a narrower format does. */
+static inline float tf32_rn(float x)
+{
+    uint32_t u = bits_of(x);
+    if ((u & 0x7F800000u) == 0x7F800000u) return x;
+    uint32_t keep_lsb = (u >> 13) & 1u;
+    u += 0x00000FFFu + keep_lsb;
+    return float_of(u & 0xFFFFE000u);
+}
+
+/* Round toward zero to TF32. */
+static inline float tf32_rz(float x) { return float_of(bits_of(x) & 0xFFFFE000u); }
+
+/* ------------------------------------------------------------------------ */
+/* Step 1: splits                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* BF16x9 split of one value into three scaled BF16 components
+ * ([Blog] Fig. 1: "each FP32 operand is split into three scaled BF16
+ * components"):  a = c0 + 2^-8 c1 + 2^-16 c2.
+ *   c0 = RZ_bf16(a)
+ *   c1 = RZ_bf16(2^8 (a - c0))
+ *   c2 = 2^8 (2^8 (a - c0) - c1)       -- at most 8 significant bits, so BF16
+ * Each subtraction is exact (the subtrahend is a leading part of the
+ * minuend) and each scaling by 2^8 is exact. */
+static inline void split3(float a, float *c0, float *c1, float *c2)
+{
+    float a0 = bf16_rz(a);
+    float r1 = (a - a0) * 256.0f;
+    float a1 = bf16_rz(r1);
+    float a2 = (r1 - a1) * 256.0f;
+    *c0 = a0; *c1 = a1; *c2 = a2;
+}
+
+/* TF32x3 split ([Blog] Fig. 2: a leading TF32 component and a residual TF32
+ * component, no scale factor). */
+enum { TF32X3_HI_RN = 0, TF32X3_HI_RZ = 1 };
+static inline void split2(float a, int variant, float *hi, float *lo)
+{
+    float h = (variant == TF32X3_HI_RZ) ? tf32_rz(a) : tf32_rn(a);
+    *hi = h;
+    *lo = tf32_rn(a - h);
+}
+
+ORACLE_API void oracle_split_bf16x9(const float *a, int64_t n,
+                                    uint16_t *s0, uint16_t *s1, uint16_t *s2)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        float c0, c1, c2;
+        split3(a[i], &c0, &c1, &c2);
+        s0[i] = (uint16_t)(bits_of(c0) >> 16);
+        s1[i] = (uint16_t)(bits_of(c1) >> 16);
+        s2[i] = (uint16_t)(bits_of(c2) >> 16);
+    }
+}
+
+/* The low 16 bits of every FP32 word written here are zero when the split is
+ * exact; the caller checks that, which is why the words are returned whole. */
+ORACLE_API void oracle_split_bf16x9_f32(const float *a, int64_t n,
+                                        float *c0, float *c1, float *c2)
+{
+    for (int64_t i = 0; i < n; ++i) split3(a[i], &c0[i], &c1[i], &c2[i]);
+}
+
+ORACLE_API void oracle_split_tf32x3(const float *a, int64_t n, int variant,
+                                    float *hi, float *lo)
+{
+    for (int64_t i = 0; i < n; ++i) split2(a[i], variant, &hi[i], &lo[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* operand packing: op(A) as M x K rows, op(B)^T as N x K rows              */
+/* (a copy, no arithmetic; it only makes the k loops below contiguous)      */
+/* ------------------------------------------------------------------------ */
+static float *pack_opA(int transA, int64_t M, int64_t K, const float *A, int64_t lda)
+{
+    float *p = (float *)malloc(sizeof(float) * (size_t)(M > 0 ? M : 1) * (size_t)(K > 0 ? K : 1));
+    if (!p) return NULL;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t k = 0; k < K; ++k)
+            p[m * K + k] = transA ? A[k * lda + m] : A[m * lda + k];
+    return p;
+}
+
+static float *pack_opBt(int transB, int64_t N, int64_t K, const float *B, int64_t ldb)
+{
+    float *p = (float *)malloc(sizeof(float) * (size_t)(N > 0 ? N : 1) * (size_t)(K > 0 ? K : 1));
+    if (!p) return NULL;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k)
+            p[n * K + k] = transB ? B[n * ldb + k] : B[k * ldb + n];
+    return p;
+}
+
+static inline int64_t row_at(const int64_t *rows, int64_t r) { return rows ? rows[r] : r; }
+
+/* C = fmaf(alpha, acc, beta*C_old) + bias, in FP32.  beta == 0 never reads C_old. */
+static inline float epilogue_f32(float acc, float alpha, float beta, const float *Cold_elem,
+                                 const float *bias_elem)
+{
+    float bc = (beta != 0.0f) ? beta * (*Cold_elem) : 0.0f;
+    float c = fmaf(alpha, acc, bc);
+    if (bias_elem) c = c + *bias_elem;
+    return c;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Plain definitions                                                         */
+/* ------------------------------------------------------------------------ */
+
+/* float64 GEMM: C64 = alpha * (op(A) op(B)) + beta * C_old + bias, every
+ * product and sum in binary64, sequential in k.  Output rows follow `rows`
+ * (C64 has nrows x N entries, row-major, leading dimension N). */
+ORACLE_API int oracle_gemm_f64(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                               double alpha, const float *A, int64_t lda,
+                               const float *B, int64_t ldb,
+                               double beta, const float *Cold, int64_t ldc,
+                               const float *bias,
+                               const int64_t *rows, int64_t nrows, double *C64)
+{
+    if (!rows) nrows = M;
+    float *pa = pack_opA(transA, M, K, A, lda);
+    float *pb = pack_opBt(transB, N, K, B, ldb);
+    if (!pa || !pb) { free(pa); free(pb); return -1; }
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t m = row_at(rows, r);
+        for (int64_t n = 0; n < N; ++n) {
+            const float *ar = pa + m * K, *br = pb + n * K;
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k) s += (double)ar[k] * (double)br[k];
+            double c = alpha * s;
+            if (beta != 0.0) c += beta * (double)Cold[m * ldc + n];
+            if (bias) c += (double)bias[n];
+            C64[r * N + n] = c;
+        }
+    }
+    free(pa); free(pb);
+    return 0;
+}
+
+/* The denominator of the normwise error: D = |alpha| (|op(A)| |op(B)|)
+ * + |beta| |C_old| + |bias|, in binary64. */
+ORACLE_API int oracle_gemm_absdenom_f64(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                                        double alpha, const float *A, int64_t lda,
+                                        const float *B, int64_t ldb,
+                                        double beta, const float *Cold, int64_t ldc,
+                                        const float *bias,
+                                        const int64_t *rows, int64_t nrows, double *D)
+{
+    if (!rows) nrows = M;
+    float *pa = pack_opA(transA, M, K, A, lda);
+    float *pb = pack_opBt(transB, N, K, B, ldb);
+    if (!pa || !pb) { free(pa); free(pb); return -1; }
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t m = row_at(rows, r);
+        for (int64_t n = 0; n < N; ++n) {
+            const float *ar = pa + m * K, *br = pb + n * K;
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k) s += fabs((double)ar[k]) * fabs((double)br[k]);
+            double d = fabs(alpha) * s;
+            if (beta != 0.0) d += fabs(beta) * fabs((double)Cold[m * ldc + n]);
+            if (bias) d += fabs((double)bias[n]);
+            D[r * N + n] = d;
+        }
+    }
+    free(pa); free(pb);
+    return 0;
+}
+
+/* Native FP32 SGEMM: acc = fmaf(a_k, b_k, acc) for k = 0..K-1 in order,
+ * then the FP32 epilogue.  C has nrows x N entries (leading dimension N). */
+ORACLE_API int oracle_sgemm_f32(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                                float alpha, const float *A, int64_t lda,
+                                const float *B, int64_t ldb,
+                                float beta, const float *Cold, int64_t ldc,
+                                const float *bias,
+                                const int64_t *rows, int64_t nrows, float *C)
+{
+    if (!rows) nrows = M;
+    float *pa = pack_opA(transA, M, K, A, lda);
+    float *pb = pack_opBt(transB, N, K, B, ldb);
+    if (!pa || !pb) { free(pa); free(pb); return -1; }
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t m = row_at(rows, r);
+        for (int64_t n = 0; n < N; ++n) {
+            const float *ar = pa + m * K, *br = pb + n * K;
+            float acc = 0.0f;
+            for (int64_t k = 0; k < K; ++k) acc = fmaf(ar[k], br[k], acc);
+            C[r * N + n] = epilogue_f32(acc, alpha, beta, Cold + m * ldc + n,
+                                        bias ? bias + n : NULL);
+        }
+    }
+    free(pa); free(pb);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Steps 2-3: BF16x9                                                         */
+/* ------------------------------------------------------------------------ */
+enum { BF16X9_FIVE_BANDS = 0, BF16X9_ONE_ACCUMULATOR = 1 };
+
+/* Split every element of an n-vector into its three scaled BF16 components,
+ * stored as three planes. */
+static float *split3_planes(const float *x, int64_t n)
+{
+    float *p = (float *)malloc(sizeof(float) * 3 * (size_t)(n > 0 ? n : 1));
+    if (!p) return NULL;
+    for (int64_t i = 0; i < n; ++i) split3(x[i], &p[i], &p[n + i], &p[2 * n + i]);
+    return p;
+}
+
+/* BF16x9 emulated GEMM ([Blog] Fig. 1).
+ *   Products: P_ij(k) = a_i(k) * b_j(k), BF16 x BF16, exact in FP32.
+ *   Band b = i + j carries the scale 2^-8b.
+ *   FIVE_BANDS (the plain reading of "accumulated in FP32 along the five
+ *   anti-diagonal bands"): S_b = sum over k of the band's products, one FP32
+ *   round-to-nearest sum per band, the products of band b added in order of
+ *   ascending i; then acc = S_4 2^-32 + S_3 2^-24 + S_2 2^-16 + S_1 2^-8 + S_0,
+ *   added smallest band first, in FP32.
+ *   ONE_ACCUMULATOR: one FP32 sum; for each k the scaled products are added
+ *   band 4 first, down to band 0.
+ * bands_out (optional, 5 x nrows x N): the band sums S_0..S_4 (FIVE_BANDS). */
+ORACLE_API int oracle_gemm_bf16x9(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                                  float alpha, const float *A, int64_t lda,
+                                  const float *B, int64_t ldb,
+                                  float beta, const float *Cold, int64_t ldc,
+                                  const float *bias, int variant,
+                                  const int64_t *rows, int64_t nrows,
+                                  float *C, float *bands_out)
+{
+    if (!rows) nrows = M;
+    float *pa = pack_opA(transA, M, K, A, lda);
+    float *pb = pack_opBt(transB, N, K, B, ldb);
+    float *sa = pa ? split3_planes(pa, M * K) : NULL;
+    float *sb = pb ? split3_planes(pb, N * K) : NULL;
+    if (!pa || !pb || !sa || !sb) { free(pa); free(pb); free(sa); free(sb); return -1; }
+    const int64_t MK = M * K, NK = N * K;
+    /* scale of band b: 2^-8b */
+    const float band_scale[5] = { 1.0f, 0x1p-8f, 0x1p-16f, 0x1p-24f, 0x1p-32f };
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t m = row_at(rows, r);
+        for (int64_t n = 0; n < N; ++n) {
+            const float *a[3] = { sa + m * K, sa + MK + m * K, sa + 2 * MK + m * K };
+            const float *b[3] = { sb + n * K, sb + NK + n * K, sb + 2 * NK + n * K };
+            float acc;
+            if (variant == BF16X9_ONE_ACCUMULATOR) {
+                acc = 0.0f;
+                for (int64_t k = 0; k < K; ++k)
+                    for (int band = 4; band >= 0; --band)
+                        for (int i = 0; i <= 2; ++i) {
+                            int j = band - i;
+                            if (j < 0 || j > 2) continue;
+                            float p = a[i][k] * b[j][k];          /* exact */
+                            acc = acc + p * band_scale[band];     /* scale exact */
+                        }
+            } else {
+                float S[5] = { 0.0f, 0.0f, 0.0f, 0.0f, 0.0f };
+                for (int64_t k = 0; k < K; ++k)
+                    for (int band = 0; band <= 4; ++band)
+                        for (int i = 0; i <= 2; ++i) {
+                            int j = band - i;
+                            if (j < 0 || j > 2) continue;
+                            S[band] = S[band] + a[i][k] * b[j][k];
+                        }
+                if (bands_out)
+                    for (int band = 0; band < 5; ++band)
+                        bands_out[(int64_t)band * nrows * N + r * N + n] = S[band];
+                acc = S[4] * band_scale[4];
+                acc = acc + S[3] * band_scale[3];
+                acc = acc + S[2] * band_scale[2];
+                acc = acc + S[1] * band_scale[1];
+                acc = acc + S[0];
+            }
+            C[r * N + n] = epilogue_f32(acc, alpha, beta, Cold + m * ldc + n,
+                                        bias ? bias + n : NULL);
+        }
+    }
+    free(pa); free(pb); free(sa); free(sb);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Steps 2-3: TF32x3                                                         */
+/* ------------------------------------------------------------------------ */
+
+/* TF32x3 emulated GEMM ([Blog] Fig. 2 and Eq. 1):
+ *   a b ~= a_hi b_hi + a_hi b_lo + a_lo b_hi   (a_lo b_lo dropped)
+ * Each product of two TF32 values (11-bit significands) is exact in FP32.
+ * One FP32 round-to-nearest sum over k; for each k the three products are
+ * added smallest first: a_lo b_hi, a_hi b_lo, a_hi b_hi.
+ * terms_out (optional, 3 x nrows x N): the three separate sums over k of
+ * a_hi b_hi, a_hi b_lo and a_lo b_hi, each accumulated in FP32 in k order. */
+ORACLE_API int oracle_gemm_tf32x3(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                                  float alpha, const float *A, int64_t lda,
+                                  const float *B, int64_t ldb,
+                                  float beta, const float *Cold, int64_t ldc,
+                                  const float *bias, int split_variant,
+                                  const int64_t *rows, int64_t nrows,
+                                  float *C, float *terms_out)
+{
+    if (!rows) nrows = M;
+    float *pa = pack_opA(transA, M, K, A, lda);
+    float *pb = pack_opBt(transB, N, K, B, ldb);
+    float *ha = (float *)malloc(sizeof(float) * 2 * (size_t)(M * K > 0 ? M * K : 1));
+    float *hb = (float *)malloc(sizeof(float) * 2 * (size_t)(N * K > 0 ? N * K : 1));
+    if (!pa || !pb || !ha || !hb) { free(pa); free(pb); free(ha); free(hb); return -1; }
+    const int64_t MK = M * K, NK = N * K;
+    for (int64_t i = 0; i < MK; ++i) split2(pa[i], split_variant, &ha[i], &ha[MK + i]);
+    for (int64_t i = 0; i < NK; ++i) split2(pb[i], split_variant, &hb[i], &hb[NK + i]);
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t m = row_at(rows, r);
+        for (int64_t n = 0; n < N; ++n) {
+            const float *ahi = ha + m * K, *alo = ha + MK + m * K;
+            const float *bhi = hb + n * K, *blo = hb + NK + n * K;
+            float acc = 0.0f, t_hh = 0.0f, t_hl = 0.0f, t_lh = 0.0f;
+            for (int64_t k = 0; k < K; ++k) {
+                float p_lh = alo[k] * bhi[k];
+                float p_hl = ahi[k] * blo[k];
+                float p_hh = ahi[k] * bhi[k];
+                acc = acc + p_lh;
+                acc = acc + p_hl;
+                acc = acc + p_hh;
+                t_hh = t_hh + p_hh; t_hl = t_hl + p_hl; t_lh = t_lh + p_lh;
+            }
+            if (terms_out) {
+                terms_out[0 * nrows * N + r * N + n] = t_hh;
+                terms_out[1 * nrows * N + r * N + n] = t_hl;
+                terms_out[2 * nrows * N + r * N + n] = t_lh;
+            }
+            C[r * N + n] = epilogue_f32(acc, alpha, beta, Cold + m * ldc + n,
+                                        bias ? bias + n : NULL);
+        }
+    }
+    free(pa); free(pb); free(ha); free(hb);
+    return 0;
+}
+
+ORACLE_API int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,47 @@
+"""Run the oracle's pins against a deliberately broken build of the oracle.
+
+Usage: python -m tests._mutant_runner <path-to-mutant.so>
+Exit status 0 means every pin passed (the mutant survived); anything else
+(an assertion, a crash) means the pins caught the planted mistake.
+"""
+import sys
+
+import numpy as np
+
+import oracle
+from tests import _bits
+from tests import test_oracle_gemm as g
+from tests import test_oracle_split as s
+
+
+def run_pins():
+    # split pins on a reduced stratified sample
+    a = _bits.f32_patterns_stratified((0x00, 0x7F), 12)
+    s._check_bf16x9(a)
+    s._check_tf32(_bits.f32_patterns_stratified((0, 1023, 0x155), 13)[::7])
+    s.test_bf16x9_split_golden()
+    s.test_tf32x3_split_golden()
+    # GEMM pins
+    for tA, tB in g.TRANS:
+        g.test_f64_gemm_against_exact_rationals(tA, tB)
+        g.test_tf32x3_gemm_against_exact_rationals(tA, tB)
+        g.test_one_hot_rows_select_exactly(tA, tB)
+        for v in (oracle.BF16X9_FIVE_BANDS, oracle.BF16X9_ONE_ACCUMULATOR):
+            g.test_bf16x9_gemm_against_exact_rationals(v, tA, tB)
+    g.test_f64_gemm_small_integers_exact_golden()
+    g.test_sgemm_f32_within_summation_bound()
+    g.test_bf16x9_bands_hold_the_nine_products()
+    g.test_tf32x3_terms_are_the_three_products()
+    g.test_tf32x3_drops_lo_times_lo_closed_form()
+    g.test_alpha_beta_bias_placement()
+    g.test_beta_zero_never_reads_c()
+    g.test_k_zero_gives_beta_c_plus_bias()
+    for seed in (0, 1, 2):
+        g.test_bf16x9_meets_or_beats_native_fp32(seed)
+
+
+if __name__ == "__main__":
+    with oracle.use_library(sys.argv[1]):
+        run_pins()
+    np.seterr(all="ignore")
+    sys.exit(0)

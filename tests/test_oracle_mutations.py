@@ -1,0 +1,64 @@
+"""Planted mistakes in the oracle must fail its pins (no GPU).
+
+Each case copies the oracle's C source, plants one plausible mistake (a
+dropped term, a wrong sign, a wrong scale, a transposed index, a wrong
+rounding), builds it, and runs every pin against it in a child process.  The
+pins must reject every mutant; the unmodified source must pass them.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTANTS = {
+    "split_scale_wrong": ("float r1 = (a - a0) * 256.0f;", "float r1 = (a - a0) * 128.0f;"),
+    "split_third_component_dropped": ("float a2 = (r1 - a1) * 256.0f;", "float a2 = (r1 - a1) * 0.0f;"),
+    "split_rounds_to_nearest": ("return float_of(bits_of(x) & 0xFFFF0000u);",
+                                "return float_of((bits_of(x) + 0x8000u) & 0xFFFF0000u);"),
+    "band4_dropped": ("for (int band = 0; band <= 4; ++band)", "for (int band = 0; band <= 3; ++band)"),
+    "band1_sign": ("acc = acc + S[1] * band_scale[1];", "acc = acc - S[1] * band_scale[1];"),
+    "band2_scale": ("0x1p-16f, 0x1p-24f", "0x1p-15f, 0x1p-24f"),
+    "one_acc_band_misplaced": ("int j = band - i;\n                            if (j < 0 || j > 2) continue;\n                            float p",
+                               "int j = (band + 1) % 5 - i;\n                            if (j < 0 || j > 2) continue;\n                            float p"),
+    "tf32_hi_lo_dropped": ("acc = acc + p_hl;", ";"),
+    "tf32_lo_times_lo_added": ("acc = acc + p_hh;", "acc = acc + p_hh; acc = acc + alo[k] * blo[k];"),
+    "tf32_ties_away": ("u += 0x00000FFFu + keep_lsb;", "u += 0x00001000u;"),
+    "opB_transposed_index": ("p[n * K + k] = transB ? B[n * ldb + k] : B[k * ldb + n];",
+                             "p[n * K + k] = transB ? B[k * ldb + n] : B[n * ldb + k];"),
+    "opA_transposed_index": ("p[m * K + k] = transA ? A[k * lda + m] : A[m * lda + k];",
+                             "p[m * K + k] = transA ? A[m * lda + k] : A[k * lda + m];"),
+    "f64_beta_sign": ("if (beta != 0.0) c += beta * (double)Cold[m * ldc + n];",
+                      "if (beta != 0.0) c -= beta * (double)Cold[m * ldc + n];"),
+    "f64_product_in_float": ("s += (double)ar[k] * (double)br[k];",
+                             "s += (double)(float)((double)ar[k] * (double)br[k]);"),
+    "sgemm_first_term_dropped": ("acc = fmaf(ar[k], br[k], acc);",
+                                 "acc = (k == 0) ? 0.0f : fmaf(ar[k], br[k], acc);"),
+    "bias_dropped": ("if (bias_elem) c = c + *bias_elem;", ";"),
+}
+
+
+def _run(so_path):
+    env = dict(os.environ, OMP_NUM_THREADS="2")
+    return subprocess.run([sys.executable, "-m", "tests._mutant_runner", so_path], cwd=ROOT,
+                          env=env, capture_output=True, text=True, timeout=600)
+
+
+def test_unmodified_oracle_passes_reduced_pins(tmp_path):
+    so = oracle.build_variant(oracle.source(), str(tmp_path / "orig.so"))
+    r = _run(so)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = oracle.source()
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    so = oracle.build_variant(src.replace(old, new), str(tmp_path / f"{name}.so"))
+    r = _run(so)
+    assert r.returncode != 0, f"mutant {name} passed every pin"
