@@ -1,0 +1,237 @@
+"""FP32 GEMM emulated on GB300 tensor cores (BF16x9 and TF32x3).
+
+Thin Python binding over the C ABI of ``libemu_gemm.so`` (see
+``include/emu_gemm.h``): the functions below carry the C names and only
+marshal arguments (device pointers, sizes, the current CUDA stream).  Every
+step of the computation runs in the library's sm_103a kernels; there is no
+Python or CPU fallback, and a missing library raises at import of the first
+call.
+
+Method: NVIDIA blog "Unlocking Tensor Core performance for machine-learning
+interatomic potentials", section "How Tensor Core FP32 bridges the hardware
+gap" (Fig. 1 BF16x9, Fig. 2 and Eq. 1 TF32x3).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "EMU_MODE_BF16X9", "EMU_MODE_TF32X3", "EMU_OP_N", "EMU_OP_T", "EmuError",
+    "emu_sgemm", "emu_linear_fwd", "emu_linear_bwd_input", "emu_status_string",
+    "emu_stream_check", "emu_split_dump", "emu_version",
+    "sgemm", "linear_fwd", "linear_bwd_input", "EmuLinearFunction", "EmuLinear",
+    "library_path", "load",
+]
+
+EMU_MODE_BF16X9 = 0
+EMU_MODE_TF32X3 = 1
+EMU_OP_N = 0
+EMU_OP_T = 1
+MODES = {"bf16x9": EMU_MODE_BF16X9, "tf32x3": EMU_MODE_TF32X3}
+
+STATUS_NAMES = {
+    0: "EMU_STATUS_SUCCESS", 1: "EMU_STATUS_INVALID_VALUE", 2: "EMU_STATUS_NOT_SUPPORTED",
+    3: "EMU_STATUS_ARCH_MISMATCH", 4: "EMU_STATUS_ALLOC_FAILED", 5: "EMU_STATUS_LAUNCH_FAILED",
+    6: "EMU_STATUS_DEVICE_TIMEOUT",
+}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+
+
+class EmuError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = int(status)
+        super().__init__(f"{what}: {STATUS_NAMES.get(self.status, self.status)}")
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libemu_gemm.so")
+
+
+def load():
+    """Load libemu_gemm.so (built in-tree by build.py); raise if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: build it with "
+                              "`python -m fp32_emulated_gemm_gb300.build` (no CPU fallback exists)")
+        L = ctypes.CDLL(path)
+        i64, i32, f32, P = ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+        L.emu_sgemm.argtypes = [i32, i32, i32, i64, i64, i64, f32, P, i64, P, i64, f32, P, i64, P]
+        L.emu_linear_fwd.argtypes = [i32, i64, i64, i64, P, P, P, P, P]
+        L.emu_linear_bwd_input.argtypes = [i32, i64, i64, i64, P, P, P, P]
+        L.emu_status_string.argtypes = [i32]
+        L.emu_status_string.restype = ctypes.c_char_p
+        L.emu_stream_check.argtypes = [P]
+        L.emu_split_dump.argtypes = [i32, i64, i64, P, i64, i32, P, P]
+        L.emu_version.argtypes = []
+        for name in ("emu_sgemm", "emu_linear_fwd", "emu_linear_bwd_input", "emu_stream_check",
+                     "emu_split_dump", "emu_version"):
+            getattr(L, name).restype = i32
+        _lib = L
+        return L
+
+
+# ------------------------------------------------------------ C names ------
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr() if hasattr(t, "data_ptr") else int(t))
+
+
+def _check(st: int, what: str) -> None:
+    if st != 0:
+        raise EmuError(st, what)
+
+
+def emu_sgemm(mode, transA, transB, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None):
+    _check(load().emu_sgemm(int(mode), int(transA), int(transB), int(M), int(N), int(K), float(alpha),
+                            _ptr(A), int(lda), _ptr(B), int(ldb), float(beta), _ptr(C), int(ldc),
+                            ctypes.c_void_p(_stream(stream))), "emu_sgemm")
+
+
+def emu_linear_fwd(mode, M, N, K, X, W, bias, Y, stream=None):
+    _check(load().emu_linear_fwd(int(mode), int(M), int(N), int(K), _ptr(X), _ptr(W), _ptr(bias), _ptr(Y),
+                                 ctypes.c_void_p(_stream(stream))), "emu_linear_fwd")
+
+
+def emu_linear_bwd_input(mode, M, N, K, dY, W, dX, stream=None):
+    _check(load().emu_linear_bwd_input(int(mode), int(M), int(N), int(K), _ptr(dY), _ptr(W), _ptr(dX),
+                                       ctypes.c_void_p(_stream(stream))), "emu_linear_bwd_input")
+
+
+def emu_status_string(status: int) -> str:
+    return load().emu_status_string(int(status)).decode()
+
+
+def emu_stream_check(stream=None) -> int:
+    return int(load().emu_stream_check(ctypes.c_void_p(_stream(stream))))
+
+
+def emu_split_dump(mode, R, Kc, X, ldx, mn_major, out, stream=None):
+    _check(load().emu_split_dump(int(mode), int(R), int(Kc), _ptr(X), int(ldx), int(mn_major), _ptr(out),
+                                 ctypes.c_void_p(_stream(stream))), "emu_split_dump")
+
+
+def emu_version() -> int:
+    return int(load().emu_version())
+
+
+# ----------------------------------------------------- tensor helpers ------
+def _mode(mode):
+    return MODES[mode] if isinstance(mode, str) else int(mode)
+
+
+def _f32_cuda(t, name):
+    import torch
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.float32):
+        raise TypeError(f"{name} must be a CUDA float32 tensor")
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D row-major tensor (unit column stride)")
+    return t
+
+
+def sgemm(A, B, *, mode="bf16x9", transA=False, transB=False, alpha=1.0, beta=0.0, C=None):
+    """C = alpha op(A) op(B) + beta C on the current stream (C allocated when None)."""
+    import torch
+    _f32_cuda(A, "A"), _f32_cuda(B, "B")
+    M, K = (A.shape[1], A.shape[0]) if transA else A.shape
+    Kb, N = (B.shape[1], B.shape[0]) if transB else B.shape
+    if Kb != K:
+        raise ValueError("inner dimensions differ")
+    if C is None:
+        C = torch.empty((M, N), device=A.device, dtype=torch.float32)
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C")
+    _f32_cuda(C, "C")
+    emu_sgemm(_mode(mode), EMU_OP_T if transA else EMU_OP_N, EMU_OP_T if transB else EMU_OP_N, M, N, K,
+              alpha, A, A.stride(0), B, B.stride(0), beta, C, C.stride(0))
+    return C
+
+
+def linear_fwd(X, W, bias=None, *, mode="bf16x9", out=None):
+    """Y = X W^T + bias (X [M,K], W [N,K], contiguous)."""
+    import torch
+    M, K = X.shape
+    N = W.shape[0]
+    Y = out if out is not None else torch.empty((M, N), device=X.device, dtype=torch.float32)
+    emu_linear_fwd(_mode(mode), M, N, K, X.contiguous(), W.contiguous(),
+                   None if bias is None else bias.contiguous(), Y)
+    return Y
+
+
+def linear_bwd_input(dY, W, *, mode="bf16x9", out=None):
+    """dX = dY W (dY [M,N], W [N,K], contiguous)."""
+    import torch
+    M, N = dY.shape
+    K = W.shape[1]
+    dX = out if out is not None else torch.empty((M, K), device=dY.device, dtype=torch.float32)
+    emu_linear_bwd_input(_mode(mode), M, N, K, dY.contiguous(), W.contiguous(), dX)
+    return dX
+
+
+def _autograd():
+    import torch
+
+    class EmuLinearFunction(torch.autograd.Function):
+        """nn.Linear with the forward and the input gradient emulated; the
+        weight gradient uses plain FP32 (TF32 off), as in the blog's
+        TF32Linear ("TF32x3 on Ampere GPUs")."""
+
+        @staticmethod
+        def forward(ctx, X, W, bias, mode):
+            ctx.save_for_backward(X, W)
+            ctx.mode = mode
+            ctx.has_bias = bias is not None
+            return linear_fwd(X, W, bias, mode=mode)
+
+        @staticmethod
+        def backward(ctx, dY):
+            X, W = ctx.saved_tensors
+            dY = dY.contiguous()
+            dX = linear_bwd_input(dY, W, mode=ctx.mode) if ctx.needs_input_grad[0] else None
+            dW = db = None
+            if ctx.needs_input_grad[1]:
+                prev = torch.backends.cuda.matmul.allow_tf32
+                torch.backends.cuda.matmul.allow_tf32 = False
+                try:
+                    dW = dY.t().mm(X)
+                finally:
+                    torch.backends.cuda.matmul.allow_tf32 = prev
+            if ctx.has_bias and ctx.needs_input_grad[2]:
+                db = dY.sum(0)
+            return dX, dW, db, None
+
+    class EmuLinear(torch.nn.Linear):
+        """Drop-in nn.Linear whose matmuls run on the emulated path."""
+
+        def __init__(self, in_features, out_features, bias=True, mode="bf16x9", **kw):
+            super().__init__(in_features, out_features, bias=bias, **kw)
+            self.mode = mode
+
+        def forward(self, x):
+            shp = x.shape
+            y = EmuLinearFunction.apply(x.reshape(-1, shp[-1]), self.weight, self.bias, self.mode)
+            return y.reshape(*shp[:-1], self.out_features)
+
+    return EmuLinearFunction, EmuLinear
+
+
+def __getattr__(name):
+    if name in ("EmuLinearFunction", "EmuLinear"):
+        f, m = _autograd()
+        globals()["EmuLinearFunction"], globals()["EmuLinear"] = f, m
+        return globals()[name]
+    raise AttributeError(name)

@@ -1,0 +1,309 @@
+// emu_gemm.cu -- host side of libemu_gemm.so: argument checks, TMA tensor
+// maps, launch of the sm_103a kernels, and the C ABI declared in
+// include/emu_gemm.h.
+//
+// The method (blog "Unlocking Tensor Core performance for machine-learning
+// interatomic potentials", "How Tensor Core FP32 bridges the hardware gap",
+// Fig. 1, Fig. 2, Eq. 1) runs entirely in the kernels of emu_kernel.cuh; this
+// file only marshals arguments.  There is no CPU fallback: without a suitable
+// GPU every entry point returns an error.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/emu_gemm.h"
+#include "emu_kernel.cuh"
+
+namespace emu {
+namespace {
+
+constexpr unsigned long long kDefaultWaitBudgetNs = 2000000000ull;  // 2 s per wait
+
+struct DeviceInfo {
+    bool ready = false;
+    int cc_major = 0, cc_minor = 0, sm_count = 0;
+    bool attrs_set = false;
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+emu_status_t device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return EMU_STATUS_LAUNCH_FAILED;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return EMU_STATUS_LAUNCH_FAILED;
+        }
+        d.ready = true;
+    }
+    if (d.cc_major != 10 || d.cc_minor != 3) return EMU_STATUS_ARCH_MISMATCH;
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+            cudaGetLastError();
+            return EMU_STATUS_LAUNCH_FAILED;
+        }
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    if (!d.attrs_set) {
+        if (cudaFuncSetAttribute(emu_gemm_kernel<MODE_BF16X9>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_bytes<MODE_BF16X9>()) != cudaSuccess ||
+            cudaFuncSetAttribute(emu_gemm_kernel<MODE_TF32X3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_bytes<MODE_TF32X3>()) != cudaSuccess) {
+            cudaGetLastError();
+            return EMU_STATUS_LAUNCH_FAILED;
+        }
+        d.attrs_set = true;
+    }
+    *out = &d;
+    return EMU_STATUS_SUCCESS;
+}
+
+// FP32 2-D tensor map over a row-major matrix with `outer` rows of `inner`
+// elements (leading dimension ld), box {box_inner, box_outer}, 128-byte
+// swizzle, zero fill outside the matrix.
+bool encode_f32_2d(CUtensorMap* map, const float* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                   uint32_t box_inner, uint32_t box_outer) {
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {ld * sizeof(float)};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// op(X) tile map: K-major operands (rows of K) load {32 k, 128 rows};
+// MN-major operands (rows of MN) load four {32 mn, 32 k} boxes.
+bool encode_operand(CUtensorMap* map, const float* X, bool mn_major, int64_t MN, int64_t K, int64_t ld) {
+    // TMA needs every extent >= 1; a zero extent never reaches here.
+    if (!mn_major) return encode_f32_2d(map, X, (uint64_t)K, (uint64_t)MN, (uint64_t)ld, BK, BM);
+    return encode_f32_2d(map, X, (uint64_t)MN, (uint64_t)K, (uint64_t)ld, 32, BK);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+__global__ void scale_kernel(int64_t M, int64_t N, float beta, float* C, int64_t ldc, const float* bias) {
+    const int64_t total = M * N;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / N, c = i % N;
+        float* e = C + r * ldc + c;
+        const float v = beta != 0.0f ? __fmul_rn(beta, *e) : 0.0f;
+        *e = __fadd_rn(v, bias ? bias[c] : 0.0f);
+    }
+}
+
+emu_status_t check_error_flag(bool clear) {
+    unsigned int flag = 0;
+    if (cudaMemcpyFromSymbol(&flag, g_error_flag, sizeof(flag)) != cudaSuccess) {
+        cudaGetLastError();
+        return EMU_STATUS_LAUNCH_FAILED;
+    }
+    if (flag && clear) {
+        const unsigned int zero = 0;
+        cudaMemcpyToSymbol(g_error_flag, &zero, sizeof(zero));
+    }
+    return flag ? EMU_STATUS_DEVICE_TIMEOUT : EMU_STATUS_SUCCESS;
+}
+
+unsigned long long wait_budget_ns() {
+    static unsigned long long v = [] {
+        const char* s = std::getenv("EMU_WAIT_BUDGET_NS");
+        unsigned long long x = s ? std::strtoull(s, nullptr, 10) : 0ull;
+        return x ? x : kDefaultWaitBudgetNs;
+    }();
+    return v;
+}
+
+// Core: C = alpha * op(A) op(B) + beta * C_old + bias, with C_old == C.
+emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t N, int64_t K, float alpha,
+                      const float* A, int64_t lda, const float* B, int64_t ldb, float beta, float* C,
+                      int64_t ldc, const float* bias, cudaStream_t stream) {
+    if (mode != EMU_MODE_BF16X9 && mode != EMU_MODE_TF32X3) return EMU_STATUS_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0) return EMU_STATUS_INVALID_VALUE;
+    if (M > INT32_MAX - 256 || N > INT32_MAX - 256 || K > INT32_MAX - 256) return EMU_STATUS_NOT_SUPPORTED;
+    if (M == 0 || N == 0) return EMU_STATUS_SUCCESS;
+    const int64_t a_rows = a_mn ? K : M, a_cols = a_mn ? M : K;
+    const int64_t b_rows = b_mn ? K : N, b_cols = b_mn ? N : K;
+    (void)a_rows; (void)b_rows;
+    if (ldc < N || !C) return EMU_STATUS_INVALID_VALUE;
+    const bool gemm = K > 0 && alpha != 0.0f;
+    if (gemm) {
+        if (!A || !B || lda < a_cols || ldb < b_cols) return EMU_STATUS_INVALID_VALUE;
+        if (!aligned16(A) || !aligned16(B) || (lda & 3) || (ldb & 3)) return EMU_STATUS_NOT_SUPPORTED;
+    }
+    if (!aligned16(C) || (ldc & 3)) return EMU_STATUS_NOT_SUPPORTED;
+    if (bias && !aligned16(bias)) return EMU_STATUS_NOT_SUPPORTED;
+
+    DeviceInfo* dev = nullptr;
+    emu_status_t st = device_info(&dev);
+    if (st != EMU_STATUS_SUCCESS) return st;
+
+    if (!gemm) {
+        const int64_t total = M * N;
+        const int threads = 256;
+        const int64_t blocks64 = (total + threads - 1) / threads;
+        const int blocks = (int)(blocks64 < dev->sm_count * 8 ? blocks64 : dev->sm_count * 8);
+        scale_kernel<<<blocks, threads, 0, stream>>>(M, N, beta, C, ldc, bias);
+        return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
+    }
+
+    Params p{};
+    if (!encode_operand(&p.tmA, A, a_mn, M, K, lda) || !encode_operand(&p.tmB, B, b_mn, N, K, ldb))
+        return EMU_STATUS_LAUNCH_FAILED;
+    p.M = (int)M; p.N = (int)N; p.K = (int)K;
+    p.a_mn_major = a_mn; p.b_mn_major = b_mn;
+    p.tiles_m = (int)((M + BM - 1) / BM);
+    p.tiles_n = (int)((N + BN - 1) / BN);
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.k_stages = (int)((K + BK - 1) / BK);
+    p.alpha = alpha; p.beta = beta;
+    p.c_old = C; p.c = C; p.ldc = ldc;
+    p.bias = bias;
+    p.wait_budget_ns = wait_budget_ns();
+    const int grid = p.num_tiles < dev->sm_count ? p.num_tiles : dev->sm_count;
+    if (mode == EMU_MODE_BF16X9)
+        emu_gemm_kernel<MODE_BF16X9><<<grid, NUM_THREADS, smem_bytes<MODE_BF16X9>(), stream>>>(p);
+    else
+        emu_gemm_kernel<MODE_TF32X3><<<grid, NUM_THREADS, smem_bytes<MODE_TF32X3>(), stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
+}
+
+// ----------------------------------------------------------- split dump ----
+template <int MODE>
+__global__ void __launch_bounds__(256, 1) split_dump_kernel(const __grid_constant__ CUtensorMap tm, int R, int Kc,
+                                                            int mn_major, void* out) {
+    using C = Cfg<MODE>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* f32 = smem;
+    uint8_t* comp = smem + FP32_TILE_BYTES;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(comp + C::NCOMP * C::COMP_TILE);
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(bar, FP32_TILE_BYTES);
+        if (!mn_major) tma_load_2d(f32, &tm, bar, 0, 0);
+        else for (int j = 0; j < 4; ++j) tma_load_2d(f32 + j * 4096, &tm, bar, 32 * j, 0);
+    }
+    volatile int no_abort = 0;
+    if (!mbar_wait_warp(bar, 0, &no_abort, 1000000000ull, 5)) return;
+    split_operand<MODE>(f32, comp, mn_major != 0, threadIdx.x);
+    __syncthreads();
+    for (int i = threadIdx.x; i < R * Kc; i += blockDim.x) {
+        const uint32_t r = i / Kc, k = i % Kc;
+        for (int c = 0; c < C::NCOMP; ++c) {
+            const uint8_t* tile = comp + c * C::COMP_TILE;
+            if constexpr (MODE == MODE_BF16X9) {
+                const uint16_t v = *reinterpret_cast<const uint16_t*>(tile + off_bf16_chunk(r, k >> 3) + (k & 7u) * 2);
+                reinterpret_cast<uint16_t*>(out)[(size_t)c * R * Kc + i] = v;
+            } else {
+                const uint32_t v = *reinterpret_cast<const uint32_t*>(tile + off_f32_chunk(r, k >> 2) + (k & 3u) * 4);
+                reinterpret_cast<uint32_t*>(out)[(size_t)c * R * Kc + i] = v;
+            }
+        }
+    }
+}
+
+}  // namespace
+}  // namespace emu
+
+using namespace emu;
+
+extern "C" {
+
+emu_status_t emu_sgemm(emu_mode_t mode, emu_op_t transA, emu_op_t transB, int64_t M, int64_t N, int64_t K,
+                       float alpha, const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
+                       float* C, int64_t ldc, emu_stream_t stream) {
+    if ((transA != EMU_OP_N && transA != EMU_OP_T) || (transB != EMU_OP_N && transB != EMU_OP_T))
+        return EMU_STATUS_INVALID_VALUE;
+    // op(A) is K-major in memory when A is stored M x K; op(B) when B is N x K.
+    return run_gemm(mode, transA == EMU_OP_T, transB == EMU_OP_N, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                    nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+emu_status_t emu_linear_fwd(emu_mode_t mode, int64_t M, int64_t N, int64_t K, const float* X, const float* W,
+                            const float* bias, float* Y, emu_stream_t stream) {
+    // Y = X W^T + b: op(A) = X (K-major), op(B) = W^T (W is N x K, K-major)
+    return run_gemm(mode, false, false, M, N, K, 1.0f, X, K, W, K, 0.0f, Y, N, bias,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+emu_status_t emu_linear_bwd_input(emu_mode_t mode, int64_t M, int64_t N, int64_t K, const float* dY,
+                                  const float* W, float* dX, emu_stream_t stream) {
+    // dX[M,K] = dY[M,N] W[N,K]: GEMM with output width K and contraction N;
+    // op(B) = W is MN-major (rows are the contraction index)
+    return run_gemm(mode, false, true, M, K, N, 1.0f, dY, N, W, K, 0.0f, dX, K, nullptr,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char* emu_status_string(emu_status_t s) {
+    switch (s) {
+        case EMU_STATUS_SUCCESS: return "EMU_STATUS_SUCCESS";
+        case EMU_STATUS_INVALID_VALUE: return "EMU_STATUS_INVALID_VALUE";
+        case EMU_STATUS_NOT_SUPPORTED: return "EMU_STATUS_NOT_SUPPORTED";
+        case EMU_STATUS_ARCH_MISMATCH: return "EMU_STATUS_ARCH_MISMATCH";
+        case EMU_STATUS_ALLOC_FAILED: return "EMU_STATUS_ALLOC_FAILED";
+        case EMU_STATUS_LAUNCH_FAILED: return "EMU_STATUS_LAUNCH_FAILED";
+        case EMU_STATUS_DEVICE_TIMEOUT: return "EMU_STATUS_DEVICE_TIMEOUT";
+    }
+    return "EMU_STATUS_UNKNOWN";
+}
+
+emu_status_t emu_stream_check(emu_stream_t stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return EMU_STATUS_LAUNCH_FAILED;
+    }
+    return check_error_flag(true);
+}
+
+emu_status_t emu_split_dump(emu_mode_t mode, int64_t R, int64_t Kc, const float* X, int64_t ldx, int mn_major,
+                            void* out, emu_stream_t stream) {
+    if (mode != EMU_MODE_BF16X9 && mode != EMU_MODE_TF32X3) return EMU_STATUS_INVALID_VALUE;
+    if (R <= 0 || R > BM || Kc <= 0 || Kc > BK || !X || !out) return EMU_STATUS_INVALID_VALUE;
+    if (ldx < (mn_major ? R : Kc)) return EMU_STATUS_INVALID_VALUE;
+    if (!aligned16(X) || (ldx & 3)) return EMU_STATUS_NOT_SUPPORTED;
+    DeviceInfo* dev = nullptr;
+    emu_status_t st = device_info(&dev);
+    if (st != EMU_STATUS_SUCCESS) return st;
+    CUtensorMap tm;
+    if (!encode_operand(&tm, X, mn_major != 0, R, Kc, ldx)) return EMU_STATUS_LAUNCH_FAILED;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int R32 = (int)R, K32 = (int)Kc;
+    if (mode == EMU_MODE_BF16X9) {
+        const uint32_t bytes = 1024 + FP32_TILE_BYTES + 3 * Cfg<MODE_BF16X9>::COMP_TILE + 64;
+        cudaFuncSetAttribute(split_dump_kernel<MODE_BF16X9>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        split_dump_kernel<MODE_BF16X9><<<1, 256, bytes, s>>>(tm, R32, K32, mn_major, out);
+    } else {
+        const uint32_t bytes = 1024 + FP32_TILE_BYTES + 2 * Cfg<MODE_TF32X3>::COMP_TILE + 64;
+        cudaFuncSetAttribute(split_dump_kernel<MODE_TF32X3>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        split_dump_kernel<MODE_TF32X3><<<1, 256, bytes, s>>>(tm, R32, K32, mn_major, out);
+    }
+    return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
+}
+
+int emu_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,151 @@
+/*
+ * emu_gemm.h -- FP32 GEMM emulated on GB300 (sm_103a) tensor cores.
+ *
+ * C ABI of libemu_gemm.so.  Two emulation modes, from the NVIDIA blog post
+ * "Unlocking Tensor Core performance for machine-learning interatomic
+ * potentials", section "How Tensor Core FP32 bridges the hardware gap":
+ *
+ *   EMU_MODE_BF16X9 (Fig. 1): every FP32 operand is split into three scaled
+ *     BF16 components; the nine pairwise component products are evaluated on
+ *     the tensor cores and accumulated in FP32 along the five anti-diagonal
+ *     bands, smallest band first.
+ *   EMU_MODE_TF32X3 (Fig. 2, Eq. 1): every operand is split into a leading
+ *     and a residual TF32 component; a*b ~= a_hi b_hi + a_hi b_lo + a_lo b_hi
+ *     (the residual*residual product is dropped), accumulated in FP32.
+ *
+ * FP32 in, FP32 out: the linear-layer entry points behave like nn.Linear, and
+ * only the inner matrix product changes (section "TF32x3 on Ampere GPUs":
+ * the layer keeps its weights, bias and shapes; the input gradient also runs
+ * emulated, because forces are derivatives of the energy).
+ *
+ * Conventions (the blog leaves these open):
+ *   - Layout: ROW-MAJOR, as in PyTorch (BLAS is column-major).  Element (i, j)
+ *     of an R x C matrix X with leading dimension ldx is X[i * ldx + j].
+ *   - op(X) = X when the op is EMU_OP_N, X^T when it is EMU_OP_T.
+ *   - Pointers: caller-owned DEVICE memory of the current CUDA device.  The
+ *     library allocates nothing on the device and keeps no pointer after the
+ *     call returns; it never frees caller memory.
+ *   - Alignment (TMA): A and B must start on a 16-byte boundary and lda, ldb
+ *     must be multiples of 4 elements; C the same (ldc multiple of 4).
+ *     Violations return EMU_STATUS_NOT_SUPPORTED.
+ *   - Execution: asynchronous on `stream` (NULL = the legacy default stream).
+ *     All argument checks happen on the host before anything is enqueued;
+ *     a call that returns an error has enqueued nothing.
+ *   - Degenerate sizes: M == 0 or N == 0 is a no-op; K == 0 or alpha == 0
+ *     gives C = beta * C (+ bias).  beta == 0 never reads C, so C may hold NaN.
+ *   - Accuracy: BF16x9 results lie within 2*K*2^-24 * (|alpha| |op(A)||op(B)|
+ *     + |beta||C| + |bias|) of the exact result, elementwise; TF32x3 within
+ *     4*K*2^-24 times the same.  Inputs must be finite: the split of an Inf
+ *     produces NaN components (Inf - Inf), so Inf is not propagated as IEEE
+ *     arithmetic would.  BF16 components below 2^-133 are lost, so inputs
+ *     with |x| < 2^-110 are represented with reduced relative precision.
+ *   - Errors: no exception crosses the ABI.  A kernel whose internal waits
+ *     time out records a device-side flag instead of hanging; it is reported
+ *     as EMU_STATUS_DEVICE_TIMEOUT by emu_stream_check() (or by the next call
+ *     on any stream).
+ *   - Thread safety: all entry points may be called concurrently from
+ *     several host threads.
+ */
+#ifndef EMU_GEMM_H
+#define EMU_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t (struct CUstream_st *); declared here so the
+ * header does not need the CUDA headers. */
+typedef struct CUstream_st *emu_stream_t;
+
+typedef enum {
+    EMU_MODE_BF16X9 = 0, /* three BF16 components, nine products, five bands (Fig. 1) */
+    EMU_MODE_TF32X3 = 1  /* two TF32 components, three products (Fig. 2, Eq. 1) */
+} emu_mode_t;
+
+typedef enum { EMU_OP_N = 0, EMU_OP_T = 1 } emu_op_t;
+
+typedef enum {
+    EMU_STATUS_SUCCESS = 0,
+    EMU_STATUS_INVALID_VALUE = 1,   /* negative size, ld too small, NULL with non-zero size, bad enum */
+    EMU_STATUS_NOT_SUPPORTED = 2,   /* pointer or leading dimension not aligned for TMA */
+    EMU_STATUS_ARCH_MISMATCH = 3,   /* current device is not compute capability 10.x (sm_100 family) */
+    EMU_STATUS_ALLOC_FAILED = 4,    /* reserved: the library does not allocate device memory */
+    EMU_STATUS_LAUNCH_FAILED = 5,   /* a CUDA call failed (no device, launch error, TMA encode error) */
+    EMU_STATUS_DEVICE_TIMEOUT = 6   /* a kernel gave up on an internal wait and returned early */
+} emu_status_t;
+
+/*
+ * emu_sgemm -- C = alpha * op(A) * op(B) + beta * C.
+ *   op(A) is M x K, op(B) is K x N, C is M x N, all FP32, row-major.
+ *   A: M x K (lda >= K) when transA == EMU_OP_N, K x M (lda >= M) when EMU_OP_T.
+ *   B: K x N (ldb >= N) when transB == EMU_OP_N, N x K (ldb >= K) when EMU_OP_T.
+ *   C: read only when beta != 0 (ldc >= N).  C must not overlap A or B.
+ * Blog: "How Tensor Core FP32 bridges the hardware gap" (Fig. 1, Fig. 2, Eq. 1);
+ * the SGEMM form is how the blog applies BF16x9 to unchanged models ("BF16x9
+ * on Blackwell GPUs").
+ */
+emu_status_t emu_sgemm(emu_mode_t mode, emu_op_t transA, emu_op_t transB,
+                       int64_t M, int64_t N, int64_t K,
+                       float alpha, const float *A, int64_t lda,
+                       const float *B, int64_t ldb,
+                       float beta, float *C, int64_t ldc, emu_stream_t stream);
+
+/*
+ * emu_linear_fwd -- Y[M,N] = X[M,K] * W[N,K]^T + bias[N]   (bias may be NULL).
+ *   X, W, Y dense row-major (leading dimensions K, K, N).  The forward pass
+ *   of a linear layer with the layer's own weight layout (nn.Linear keeps W
+ *   as out_features x in_features).  Blog: "TF32x3 on Ampere GPUs" (the
+ *   layer keeps FP32 weights, bias and shapes; only the matmul changes).
+ */
+emu_status_t emu_linear_fwd(emu_mode_t mode, int64_t M, int64_t N, int64_t K,
+                            const float *X, const float *W, const float *bias,
+                            float *Y, emu_stream_t stream);
+
+/*
+ * emu_linear_bwd_input -- dX[M,K] = dY[M,N] * W[N,K].
+ *   The input-gradient pass of the same layer, emulated as well (blog,
+ *   "TF32x3 on Ampere GPUs": forces are derivatives of the energy, so the
+ *   gradient to the layer input uses the emulated arithmetic too).  All
+ *   operands dense row-major.  The weight gradient is not part of the
+ *   library (the blog computes it with standard FP32).
+ */
+emu_status_t emu_linear_bwd_input(emu_mode_t mode, int64_t M, int64_t N, int64_t K,
+                                  const float *dY, const float *W, float *dX,
+                                  emu_stream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *emu_status_string(emu_status_t s);
+
+/*
+ * emu_stream_check -- synchronise `stream`, then report and clear the
+ * device-side timeout flag of the current device: EMU_STATUS_DEVICE_TIMEOUT
+ * if a kernel gave up on a wait since the last check, EMU_STATUS_LAUNCH_FAILED
+ * on a CUDA error, EMU_STATUS_SUCCESS otherwise.
+ */
+emu_status_t emu_stream_check(emu_stream_t stream);
+
+/*
+ * emu_split_dump -- diagnostic: run the kernels' own operand split on an
+ * R x Kc FP32 matrix X (row-major, ldx, device memory; Kc <= 32 columns of
+ * one k-block) and write the components the MMA would read, as raw bit
+ * patterns, to `out` (device memory):
+ *   BF16X9: 3 planes of R x Kc uint16 (BF16 words, band scale applied:
+ *           component i equals the scaled component times 2^-8i);
+ *   TF32X3: 2 planes of R x Kc uint32 (hi, lo as FP32 words).
+ * mn_major != 0 feeds X through the transposing (MN-major) split path as
+ * the K x R matrix X^T stored row-major with ldx >= R.
+ * R <= 128.  Same alignment rules as emu_sgemm.
+ */
+emu_status_t emu_split_dump(emu_mode_t mode, int64_t R, int64_t Kc, const float *X, int64_t ldx,
+                            int mn_major, void *out, emu_stream_t stream);
+
+/* Library version as an integer (major * 10000 + minor * 100 + patch). */
+int emu_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EMU_GEMM_H */
