@@ -1,0 +1,367 @@
+"""Benchmark: effective FP32 TFLOPS of the emulated GEMMs on PET-shaped layers.
+
+One step = the hot path over one batch: the forward GEMM of a PET-like linear
+layer, Y = X W^T + b (M = 6144 tokens = 192 atoms x 32 neighbours, K = 256,
+N = 1024), and its input-gradient GEMM dX = dY W, both through the C ABI
+(emu_linear_fwd, emu_linear_bwd_input).  Effective FLOPs = 2 M N K per GEMM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--mode bf16x9|tf32x3]
+                    [--workload pet_small|pet_large|wide_l1|wide_l2] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Inputs are synthetic (seeded; X ~ N(0,1),
+W ~ N(0,1/K), b ~ N(0,0.01), dY ~ N(0,1)).  The L2 cache (129 MB) is flushed
+between timed steps by writing a 256 MB buffer; step times are CUDA-event
+device times of the two GEMM launches on the launching stream.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "effective FP32 TFLOPS (BF16x9 GEMM, PET shapes) and % of BF16-peak/9 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--mode", default="bf16x9", choices=["bf16x9", "tf32x3"])
+    ap.add_argument("--workload", default="pet_small", choices=["pet_small", "pet_large", "wide_l1", "wide_l2"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def shape_of(name):
+    from fp32_emulated_gemm_gb300 import workloads as W
+    return {"pet_small": W.PET_SMALL, "pet_large": W.PET_LARGE, "wide_l1": W.WIDE_L1, "wide_l2": W.WIDE_L2}[name]
+
+
+def config_id(name):
+    return {"pet_small": 2, "pet_large": 3, "wide_l1": 4, "wide_l2": 4}[name]
+
+
+def step_flops(s):
+    return 2 * (2.0 * s.M * s.N * s.K)  # forward + input gradient
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if args.impl == "ours":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(shape, mode, target_s=10.0):
+    """The CPU oracle on a bounded row sample of the same step (forward + input
+    gradient on the first r rows), timed on this host's cores."""
+    import numpy as np
+    import oracle
+    from fp32_emulated_gemm_gb300 import workloads as W
+    oracle.build()
+    X, Wt, b, dY = W.linear_inputs(shape, config_id_for_shape(shape), rows=min(shape.M, 4096))
+
+    def run(r):
+        t = time.perf_counter()
+        oracle.gemm_emulated(oracle.Problem(X[:r], Wt, transB=True, bias=b), mode)
+        oracle.gemm_emulated(oracle.Problem(dY[:r], Wt), mode)
+        return time.perf_counter() - t
+
+    r = 16
+    dt = run(r)
+    while dt < target_s / 4 and r < X.shape[0]:
+        r = min(X.shape[0], r * 4)
+        dt = run(r)
+    flops = 2 * (2.0 * r * shape.N * shape.K)
+    return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"forward + input gradient on the first {r} of {shape.M} rows ({mode}), {dt:.2f} s"}
+
+
+def config_id_for_shape(shape):
+    return {"pet_small": 2, "pet_large": 3, "wide_l1": 4, "wide_l2": 4}[shape.name]
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the CPU oracle (as it stands) on this host's cores,
+    one bounded row sample of the workload per step."""
+    if rank != 0:
+        return
+    import oracle
+    from fp32_emulated_gemm_gb300 import workloads as W
+    oracle.build()
+    s = shape_of(args.workload)
+    X, Wt, b, dY = W.linear_inputs(s, config_id(args.workload), rows=64)
+    r = 8  # rows per step: keeps --steps K runs within minutes
+
+    def step():
+        oracle.gemm_emulated(oracle.Problem(X[:r], Wt, transB=True, bias=b), args.mode)
+        oracle.gemm_emulated(oracle.Problem(dY[:r], Wt), args.mode)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t
+    flops = 2 * (2.0 * r * s.N * s.K) * args.steps
+    v = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(args, s),
+        "cpu_baseline": {"value": v, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{r} of {s.M} rows of the forward and input-gradient GEMMs per step"},
+        "e2e": {"value": v, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(args, s):
+    return {"workload": f"{s.name}: Y = X W^T + b and dX = dY W, M={s.M} K={s.K} N={s.N}",
+            "mode": args.mode, "M": s.M, "K": s.K, "N": s.N, "gemms_per_step": 2,
+            "l2": "flushed between timed steps (256 MB write)", "parallelism": f"replicas x{args.gpus}"}
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_init(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import numpy as np
+    import torch
+    import fp32_emulated_gemm_gb300 as emu
+    from fp32_emulated_gemm_gb300 import build as emu_build
+    from fp32_emulated_gemm_gb300 import workloads as W
+
+    emu_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    s = shape_of(args.workload)
+    mode = emu.MODES[args.mode]
+    X, Wt, b, dY = W.linear_inputs(s, config_id(args.workload))
+    Xd, Wd, bd, dYd = (torch.from_numpy(a).to(dev) for a in (X, Wt, b, dY))
+    Yd = torch.empty((s.M, s.N), device=dev)
+    dXd = torch.empty((s.M, s.K), device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    def fwd():
+        emu.emu_linear_fwd(mode, s.M, s.N, s.K, Xd, Wd, bd, Yd, sp)
+
+    def bwd():
+        emu.emu_linear_bwd_input(mode, s.M, s.N, s.K, dYd, Wd, dXd, sp)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1.0)
+        fwd()
+        bwd()
+    st = emu.emu_stream_check(sp)
+    if st != 0:
+        raise RuntimeError(emu.emu_status_string(st))
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sampler = ClockSampler(local)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    time.sleep(0.15)
+    t_wall = time.perf_counter()
+    for i in range(K):
+        flush.fill_(float(i & 7))
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    st = emu.emu_stream_check(sp)
+    if st != 0:
+        raise RuntimeError(emu.emu_status_string(st))
+    t_fwd = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    t_bwd = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    step_ms = sum(t_fwd) / K + sum(t_bwd) / K
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    flops = step_flops(s)
+    value = world * flops / (step_ms * 1e-3) / 1e12
+
+    peaks, peak_kind = load_peaks()
+    peak = peaks["bf16_tflops"] / (9.0 if args.mode == "bf16x9" else 6.0)
+    # dominant kernel: the emulated-GEMM kernel (both launches of a step);
+    # algorithmic work per launch = 2 M N K effective FLOPs
+    achieved = (flops / 2) / ((step_ms / 2) * 1e-3) / 1e12
+    traffic = load_traffic(args)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(emu, mode, s, X, Wt, b, dY, dev, stream, n=max(5, min(K, 50)))
+        if world > 1:
+            t = torch.tensor([e2e["ms"]], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e["ms"] = float(t.item())
+        e2e = {"value": world * flops / (e2e["ms"] * 1e-3) / 1e12, "unit": "TFLOPS",
+               "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16x9" if args.mode == "bf16x9" else "tf32x3", "data": "synthetic",
+        "config": workload_config(args, s),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_kind} bf16 dense burst / {9 if args.mode == 'bf16x9' else 6}",
+                     "kernel": f"emu_gemm_kernel<{args.mode}>", "fwd_ms": sum(t_fwd) / K,
+                     "bwd_ms": sum(t_bwd) / K},
+        "gpu_launches": 2 * K,
+        "wall_s_timed_region": wall,
+    }
+    if clocks:
+        line["clocks"] = clocks
+    if e2e:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(s, args.mode)
+    print(json.dumps(line), flush=True)
+
+
+def load_traffic(args):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary for this workload, or None when no capture matches the kernel."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{args.workload}_{args.mode}.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def run_e2e(emu, mode, s, X, Wt, b, dY, dev, stream, n):
+    """Same step through the public API from pinned host buffers: H2D of the
+    step's inputs, both GEMMs, D2H of both results, every step."""
+    import torch
+    hX, hW, hb, hdY = (torch.from_numpy(a).pin_memory() for a in (X, Wt, b, dY))
+    hY = torch.empty((s.M, s.N)).pin_memory()
+    hdX = torch.empty((s.M, s.K)).pin_memory()
+    Xd, Wd, bd, dYd = (torch.empty_like(t, device=dev) for t in (hX, hW, hb, hdY))
+    Yd = torch.empty((s.M, s.N), device=dev)
+    dXd = torch.empty((s.M, s.K), device=dev)
+    sp = stream.cuda_stream
+
+    def step():
+        for d, h in ((Xd, hX), (Wd, hW), (bd, hb), (dYd, hdY)):
+            d.copy_(h, non_blocking=True)
+        emu.emu_linear_fwd(mode, s.M, s.N, s.K, Xd, Wd, bd, Yd, sp)
+        emu.emu_linear_bwd_input(mode, s.M, s.N, s.K, dYd, Wd, dXd, sp)
+        hY.copy_(Yd, non_blocking=True)
+        hdX.copy_(dXd, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    h2d = sum(t.numel() * 4 for t in (hX, hW, hb, hdY))
+    d2h = (hY.numel() + hdX.numel()) * 4
+    return {"ms": e0.elapsed_time(e1) / n, "h2d": h2d, "d2h": d2h}
+
+
+if __name__ == "__main__":
+    main()

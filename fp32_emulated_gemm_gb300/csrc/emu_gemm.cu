@@ -28,7 +28,22 @@ struct DeviceInfo {
     bool ready = false;
     int cc_major = 0, cc_minor = 0, sm_count = 0;
     bool attrs_set = false;
+    int max_clusters[2] = {0, 0};  // co-resident CTA pairs per mode
 };
+
+// Split-K workspace: partial tiles plus per-tile counters, owned by the
+// library, one per (device, stream) so that calls on different streams never
+// share it.  Grown on demand, kept until the process exits.
+struct Workspace {
+    int device = -1;
+    cudaStream_t stream = nullptr;
+    float* partials = nullptr;
+    size_t partial_floats = 0;
+    int* counters = nullptr;
+    size_t num_counters = 0;
+};
+constexpr int kMaxWorkspaces = 64;
+Workspace g_ws[kMaxWorkspaces];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
@@ -71,6 +86,22 @@ emu_status_t device_info(DeviceInfo** out) {
             cudaGetLastError();
             return EMU_STATUS_LAUNCH_FAILED;
         }
+        // how many CTA pairs can be resident at once (the persistent grid)
+        for (int m = 0; m < 2; ++m) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * (d.sm_count / 2), 1, 1);
+            cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+            cfg.dynamicSmemBytes = m == 0 ? smem_bytes<MODE_BF16X9>() : smem_bytes<MODE_TF32X3>();
+            int n = 0;
+            const cudaError_t e = m == 0
+                ? cudaOccupancyMaxActiveClusters(&n, emu_gemm_kernel<MODE_BF16X9>, &cfg)
+                : cudaOccupancyMaxActiveClusters(&n, emu_gemm_kernel<MODE_TF32X3>, &cfg);
+            if (e != cudaSuccess || n <= 0) {
+                cudaGetLastError();
+                n = d.sm_count / 2;
+            }
+            d.max_clusters[m] = n;
+        }
         d.attrs_set = true;
     }
     *out = &d;
@@ -95,7 +126,7 @@ bool encode_f32_2d(CUtensorMap* map, const float* base, uint64_t inner, uint64_t
 // MN-major operands (rows of MN) load four {32 mn, 32 k} boxes.
 bool encode_operand(CUtensorMap* map, const float* X, bool mn_major, int64_t MN, int64_t K, int64_t ld) {
     // TMA needs every extent >= 1; a zero extent never reaches here.
-    if (!mn_major) return encode_f32_2d(map, X, (uint64_t)K, (uint64_t)MN, (uint64_t)ld, BK, BM);
+    if (!mn_major) return encode_f32_2d(map, X, (uint64_t)K, (uint64_t)MN, (uint64_t)ld, BK, HALF);
     return encode_f32_2d(map, X, (uint64_t)MN, (uint64_t)K, (uint64_t)ld, 32, BK);
 }
 
@@ -122,6 +153,77 @@ emu_status_t check_error_flag(bool clear) {
         cudaMemcpyToSymbol(g_error_flag, &zero, sizeof(zero));
     }
     return flag ? EMU_STATUS_DEVICE_TIMEOUT : EMU_STATUS_SUCCESS;
+}
+
+// The workspace for (current device, stream), at least `floats` partial
+// floats and `counters` zeroed counters.  Allocation happens only when the
+// cached one is too small; the counters are zeroed on the stream.
+emu_status_t workspace_for(int dev, cudaStream_t stream, size_t floats, size_t counters, Workspace** out) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    Workspace* w = nullptr;
+    for (auto& c : g_ws)
+        if (c.device == dev && c.stream == stream) { w = &c; break; }
+    if (!w)
+        for (auto& c : g_ws)
+            if (c.device < 0) { w = &c; w->device = dev; w->stream = stream; break; }
+    if (!w) return EMU_STATUS_ALLOC_FAILED;
+    if (w->partial_floats < floats) {
+        if (w->partials) cudaFreeAsync(w->partials, stream);
+        w->partials = nullptr;
+        w->partial_floats = 0;
+        if (cudaMallocAsync(reinterpret_cast<void**>(&w->partials), floats * sizeof(float), stream) != cudaSuccess) {
+            cudaGetLastError();
+            return EMU_STATUS_ALLOC_FAILED;
+        }
+        w->partial_floats = floats;
+    }
+    if (w->num_counters < counters) {
+        if (w->counters) cudaFreeAsync(w->counters, stream);
+        w->counters = nullptr;
+        w->num_counters = 0;
+        if (cudaMallocAsync(reinterpret_cast<void**>(&w->counters), counters * sizeof(int), stream) != cudaSuccess ||
+            cudaMemsetAsync(w->counters, 0, counters * sizeof(int), stream) != cudaSuccess) {
+            cudaGetLastError();
+            return EMU_STATUS_ALLOC_FAILED;
+        }
+        w->num_counters = counters;
+    }
+    *out = w;
+    return EMU_STATUS_SUCCESS;
+}
+
+// Pieces per tile.  Cost model in units of one pipeline stage (measured on
+// GB300): every unit pays its k-stages plus about 3 stages of output stores
+// (final tile or partial); a split tile's last piece also re-reads the other
+// pieces' partials (about 1.5 stages each) and stores the final tile.  Units
+// run in waves over the resident CTA pairs.
+int choose_split_k(int tiles, int k_stages, int pairs) {
+    const char* env = std::getenv("EMU_SPLIT_K");
+    if (env) {
+        const int v = std::atoi(env);
+        if (v >= 1) return v < k_stages ? v : k_stages;
+    }
+    int best = 1;
+    double best_cost = -1.0;
+    for (int S = 1; S <= 8 && S <= k_stages; ++S) {
+        if (S > 1 && k_stages / S < 2) break;
+        const long long units = (long long)tiles * S;
+        const long long waves = (units + pairs - 1) / pairs;
+        const long long per = (k_stages + S - 1) / S;
+        double cost = (double)waves * (double)(per + 3);
+        if (S > 1) cost += 1.5 * (S - 1) + 3.0;
+        if (best_cost < 0 || cost < best_cost - 1e-9) { best_cost = cost; best = S; }
+    }
+    return best;
+}
+
+// EMU_LOG=1 prints each launch's plan (tiles, split, grid) to stderr.
+bool log_enabled() {
+    static const bool on = [] {
+        const char* s = std::getenv("EMU_LOG");
+        return s && s[0] && s[0] != '0';
+    }();
+    return on;
 }
 
 unsigned long long wait_budget_ns() {
@@ -171,15 +273,35 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
         return EMU_STATUS_LAUNCH_FAILED;
     p.M = (int)M; p.N = (int)N; p.K = (int)K;
     p.a_mn_major = a_mn; p.b_mn_major = b_mn;
-    p.tiles_m = (int)((M + BM - 1) / BM);
-    p.tiles_n = (int)((N + BN - 1) / BN);
+    p.tiles_m = (int)((M + TILE_M - 1) / TILE_M);
+    p.tiles_n = (int)((N + TILE_N - 1) / TILE_N);
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.k_stages = (int)((K + BK - 1) / BK);
+    const int pairs = dev->max_clusters[mode == EMU_MODE_BF16X9 ? 0 : 1];
+    p.split_k = choose_split_k(p.num_tiles, p.k_stages, pairs);
+    p.num_units = p.num_tiles * p.split_k;
     p.alpha = alpha; p.beta = beta;
     p.c_old = C; p.c = C; p.ldc = ldc;
     p.bias = bias;
     p.wait_budget_ns = wait_budget_ns();
-    const int grid = p.num_tiles < dev->sm_count ? p.num_tiles : dev->sm_count;
+    if (p.split_k > 1) {
+        int devid = 0;
+        cudaGetDevice(&devid);
+        Workspace* w = nullptr;
+        const size_t floats = (size_t)p.num_tiles * p.split_k * TILE_M * TILE_N;
+        st = workspace_for(devid, stream, floats, (size_t)p.num_tiles * 2, &w);
+        if (st != EMU_STATUS_SUCCESS) return st;
+        p.workspace = w->partials;
+        p.counters = w->counters;
+    }
+    const int clusters = p.num_units < pairs ? p.num_units : pairs;
+    const dim3 grid(2 * clusters, 1, 1);
+    if (log_enabled())
+        std::fprintf(stderr, "[emu] %s M=%lld N=%lld K=%lld a_mn=%d b_mn=%d tiles=%dx%d k_stages=%d split_k=%d "
+                             "units=%d pairs=%d (max %d) smem=%u\n",
+                     mode == EMU_MODE_BF16X9 ? "bf16x9" : "tf32x3", (long long)M, (long long)N, (long long)K,
+                     (int)a_mn, (int)b_mn, p.tiles_m, p.tiles_n, p.k_stages, p.split_k, p.num_units, clusters,
+                     pairs, mode == EMU_MODE_BF16X9 ? smem_bytes<MODE_BF16X9>() : smem_bytes<MODE_TF32X3>());
     if (mode == EMU_MODE_BF16X9)
         emu_gemm_kernel<MODE_BF16X9><<<grid, NUM_THREADS, smem_bytes<MODE_BF16X9>(), stream>>>(p);
     else
@@ -209,7 +331,7 @@ __global__ void __launch_bounds__(256, 1) split_dump_kernel(const __grid_constan
     }
     volatile int no_abort = 0;
     if (!mbar_wait_warp(bar, 0, &no_abort, 1000000000ull, 5)) return;
-    split_operand<MODE>(f32, comp, mn_major != 0, threadIdx.x);
+    split_operand<MODE, 256>(f32, comp, mn_major != 0, threadIdx.x);
     __syncthreads();
     for (int i = threadIdx.x; i < R * Kc; i += blockDim.x) {
         const uint32_t r = i / Kc, k = i % Kc;
@@ -282,7 +404,7 @@ emu_status_t emu_stream_check(emu_stream_t stream) {
 emu_status_t emu_split_dump(emu_mode_t mode, int64_t R, int64_t Kc, const float* X, int64_t ldx, int mn_major,
                             void* out, emu_stream_t stream) {
     if (mode != EMU_MODE_BF16X9 && mode != EMU_MODE_TF32X3) return EMU_STATUS_INVALID_VALUE;
-    if (R <= 0 || R > BM || Kc <= 0 || Kc > BK || !X || !out) return EMU_STATUS_INVALID_VALUE;
+    if (R <= 0 || R > HALF || Kc <= 0 || Kc > BK || !X || !out) return EMU_STATUS_INVALID_VALUE;
     if (ldx < (mn_major ? R : Kc)) return EMU_STATUS_INVALID_VALUE;
     if (!aligned16(X) || (ldx & 3)) return EMU_STATUS_NOT_SUPPORTED;
     DeviceInfo* dev = nullptr;

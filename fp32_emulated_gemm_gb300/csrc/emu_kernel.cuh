@@ -7,25 +7,36 @@
 // tensor cores evaluate the selected component products, and accumulate in
 // FP32 (BF16x9: along five anti-diagonal bands; TF32x3: Eq. 1, lo*lo dropped).
 //
-// One persistent kernel, warp-specialised, one CTA per SM:
-//   warp 0      TMA producer: FP32 tiles of op(A) and op(B), 32 k-values per
-//               stage, into a ring of shared-memory stages (zero fill beyond
-//               the matrix edges).
-//   warp 1      MMA issuer: owns TMEM; for every stage issues the component
-//               products (18 BF16 MMAs of K=16, or 12 TF32 MMAs of K=8) into
-//               a fresh TMEM accumulator, smallest band first.
-//   warps 2-9   split warps: read the FP32 stage and write the components in
+// One persistent kernel on CTA pairs (clusters of 2, one CTA per SM).  A pair
+// computes a 256 x 256 tile of C with 2-SM tensor-core MMAs (cta_group::2):
+// CTA r of the pair holds rows [128r, 128r+128) of the tile's op(A) block and
+// rows [128r, 128r+128) of its op(B)^T block; each SM's tensor core reads its
+// own A half and both B halves, and writes its 128 x 256 quarter of the
+// accumulator to its own TMEM.  Per CTA (16 warps):
+//   warp 0      TMA producer: FP32 tiles (128 x 32 of op(A), 128 x 32 of
+//               op(B)) into a ring of shared-memory stages, zero fill beyond
+//               the matrix edges.
+//   warp 1      TMEM owner; in the leader CTA also the MMA issuer: for every
+//               32-k stage it issues the component products (18 BF16 MMAs of
+//               K=16, or 12 TF32 MMAs of K=8) into a fresh TMEM accumulator,
+//               smallest band first.
+//   warps 2-7   split warps: read the FP32 stage and write the components in
 //               the tensor cores' K-major swizzled layout (transposing when
 //               the operand is MN-major in memory).
-//   warps 10-17 epilogue: after every stage, read the stage's partial sum
-//               from TMEM and add it into FP32 registers (round to nearest),
-//               then apply alpha, beta and the bias and store the tile.
+//   warps 8-15  epilogue: after every stage, read the stage's partial sums
+//               from TMEM and add them into FP32 registers (round to
+//               nearest); at the end apply alpha, beta and the bias and store.
 //
-// Promoting each 32-k partial out of TMEM keeps the tensor core's truncating
-// block additions confined to short chains that start from zero, so the
-// result is as accurate as the blog's claim requires (BF16x9 at least as
-// accurate as native FP32 against an FP64 reference, "Limitations and
-// decision criteria").
+// Promoting each 32-k partial out of TMEM confines the tensor core's
+// truncating block additions to short chains that start from zero, so the
+// result is at least as accurate as native FP32 against an FP64 reference,
+// as the blog reports for BF16x9 ("Limitations and decision criteria").
+//
+// Split-K: when there are too few tiles to fill the GPU, a tile's k-range is
+// cut into S pieces processed by different pairs.  Each piece writes its
+// partial tile to a workspace; the last piece to finish (per-tile counter)
+// adds the S partials in the fixed order 0..S-1 -- the result does not depend
+// on which piece finishes last -- and applies the epilogue.
 #pragma once
 
 #include <cstdint>
@@ -37,46 +48,51 @@ namespace emu {
 
 enum Mode : int { MODE_BF16X9 = 0, MODE_TF32X3 = 1 };
 
-constexpr int BM = 128;  // rows of op(A) per tile (TMEM lanes)
-constexpr int BN = 128;  // columns of op(B) per tile (TMEM columns per accumulator)
-constexpr int BK = 32;   // k-values per pipeline stage
-constexpr int NUM_THREADS = 576;
+constexpr int TILE_M = 256;       // rows of a pair tile (128 per CTA)
+constexpr int TILE_N = 256;       // columns of a pair tile (TMEM columns per accumulator)
+constexpr int HALF = 128;         // rows of op(A) and of op(B)^T held by one CTA
+constexpr int BK = 32;            // k-values per pipeline stage
+constexpr int NUM_THREADS = 512;
 constexpr int WARP_PRODUCER = 0;
 constexpr int WARP_MMA = 1;
 constexpr int WARP_SPLIT0 = 2;
-constexpr int NUM_SPLIT_WARPS = 8;
-constexpr int WARP_EPI0 = WARP_SPLIT0 + NUM_SPLIT_WARPS;  // 10
+constexpr int NUM_SPLIT_WARPS = 6;
+constexpr int NUM_SPLIT_THREADS = NUM_SPLIT_WARPS * 32;
+constexpr int WARP_EPI0 = 8;
 constexpr int NUM_EPI_WARPS = 8;
-constexpr uint32_t TMEM_COLS = 2 * BN;  // two accumulators, double-buffered
+constexpr uint32_t TMEM_COLS = 2 * TILE_N;  // two accumulators, double-buffered (all 512)
+constexpr uint32_t EPI_BARRIER = 1;         // named barrier of the 256 epilogue threads
+constexpr uint32_t SPLIT_BARRIER = 2;       // named barrier of the split threads
+constexpr uint32_t STAGE_OUT_BYTES = 32 * 32 * 4;  // one epilogue warp's 32 x 32 output block
 
-// FP32 stage: op(A) tile then op(B) tile, 128 rows x 128 bytes each.
-constexpr uint32_t FP32_TILE_BYTES = 128 * BK * 4;       // 16 KB
-constexpr uint32_t FP32_STAGE_BYTES = 2 * FP32_TILE_BYTES;  // 32 KB
+// FP32 stage of one CTA: its op(A) half-tile then its op(B) half-tile.
+constexpr uint32_t FP32_TILE_BYTES = HALF * BK * 4;           // 16 KB
+constexpr uint32_t FP32_STAGE_BYTES = 2 * FP32_TILE_BYTES;    // 32 KB
 
 template <int MODE> struct Cfg;
 template <> struct Cfg<MODE_BF16X9> {
     static constexpr int NCOMP = 3;                  // components per operand
     static constexpr uint32_t ROW_BYTES = BK * 2;    // 64: one BF16 row of a stage
-    static constexpr uint32_t COMP_TILE = 128 * ROW_BYTES;          // 8 KB
+    static constexpr uint32_t COMP_TILE = HALF * ROW_BYTES;         // 8 KB
     static constexpr uint32_t SLICE_STAGE = 2 * NCOMP * COMP_TILE;  // 48 KB
     static constexpr int NF = 3;                     // FP32 stages
     static constexpr int NS = 2;                     // component stages
-    static constexpr uint32_t IDESC = make_idesc(1, BM, BN);
+    static constexpr uint32_t IDESC = make_idesc(1, TILE_M, TILE_N);
 };
 template <> struct Cfg<MODE_TF32X3> {
     static constexpr int NCOMP = 2;
     static constexpr uint32_t ROW_BYTES = BK * 4;    // 128
-    static constexpr uint32_t COMP_TILE = 128 * ROW_BYTES;          // 16 KB
+    static constexpr uint32_t COMP_TILE = HALF * ROW_BYTES;         // 16 KB
     static constexpr uint32_t SLICE_STAGE = 2 * NCOMP * COMP_TILE;  // 64 KB
     static constexpr int NF = 2;
     static constexpr int NS = 2;
-    static constexpr uint32_t IDESC = make_idesc(2, BM, BN);
+    static constexpr uint32_t IDESC = make_idesc(2, TILE_M, TILE_N);
 };
 
 template <int MODE>
 constexpr uint32_t smem_bytes() {
-    return 1024 /* alignment slack */ + Cfg<MODE>::NF * FP32_STAGE_BYTES +
-           Cfg<MODE>::NS * Cfg<MODE>::SLICE_STAGE + 1024 /* barriers and flags */;
+    return 1024 /* alignment slack */ + Cfg<MODE>::NF * FP32_STAGE_BYTES + Cfg<MODE>::NS * Cfg<MODE>::SLICE_STAGE +
+           NUM_EPI_WARPS * STAGE_OUT_BYTES + 1024 /* barriers and flags */;
 }
 
 struct Params {
@@ -85,21 +101,21 @@ struct Params {
     int M, N, K;
     int a_mn_major, b_mn_major;
     int tiles_m, tiles_n, num_tiles, k_stages;
+    int split_k;      // pieces per tile (1 = no split)
+    int num_units;    // num_tiles * split_k
     float alpha, beta;
     const float* c_old;  // read only when beta != 0
     float* c;
     long long ldc;
     const float* bias;   // may be null
+    float* workspace;    // split_k > 1: num_tiles * split_k partial tiles of 256 x 256 (thread-major)
+    int* counters;       // split_k > 1: 2 per tile, zero between launches
     unsigned long long wait_budget_ns;
 };
 
 // ----------------------------------------------------------- the splits ----
-// Byte offset of element (row, k) of an FP32 tile stored K-major with
-// 128-byte rows and the 128-byte swizzle (16-byte chunk index XOR row % 8).
-__device__ __forceinline__ uint32_t off_f32_kmajor(uint32_t row, uint32_t k) {
-    return row * 128u + ((((k >> 2) ^ row) & 7u) << 4) + ((k & 3u) << 2);
-}
-// Same for an MN-major FP32 tile: four 32-wide MN blocks of 32 k-rows each.
+// Byte offset of element (mn, k) of an MN-major FP32 tile: four 32-wide MN
+// blocks of 32 k-rows of 128 bytes, 128-byte swizzle (chunk XOR k % 8).
 __device__ __forceinline__ uint32_t off_f32_mnmajor(uint32_t mn, uint32_t k) {
     return (mn >> 5) * 4096u + k * 128u + (((((mn & 31u) >> 2) ^ k) & 7u) << 4) + ((mn & 3u) << 2);
 }
@@ -154,84 +170,69 @@ __device__ __forceinline__ void split_tf32x3_1(float x, uint32_t& hi, uint32_t& 
     lo = tf32_rn_bits(__float_as_uint(__fsub_rn(x, __uint_as_float(hi))));
 }
 
-// Split one operand tile (128 rows x 32 k) of a stage.  `src` is the FP32
-// tile, `dst` the first component tile (components follow at COMP_TILE
-// strides).  `t` is the thread's index among the 256 split threads.
 template <int MODE>
-__device__ __forceinline__ void split_operand(const uint8_t* src, uint8_t* dst, bool mn_major, uint32_t t) {
+__device__ __forceinline__ void store_components(uint8_t* dst, uint32_t row, uint32_t g, const float (&x)[8]) {
     using C = Cfg<MODE>;
-    const uint32_t lane = t & 31u, warp = t >> 5;
-    if (!mn_major) {
-        // item = (row, 8-k group): lanes cover 8 rows x 4 groups per warp
+    if constexpr (MODE == MODE_BF16X9) {
+        uint4 s0, s1, s2;
+        split_bf16x9_8(x, s0, s1, s2);
+        const uint32_t o = off_bf16_chunk(row, g);
+        *reinterpret_cast<uint4*>(dst + o) = s0;
+        *reinterpret_cast<uint4*>(dst + C::COMP_TILE + o) = s1;
+        *reinterpret_cast<uint4*>(dst + 2 * C::COMP_TILE + o) = s2;
+    } else {
+        uint32_t h[8], l[8];
 #pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const uint32_t item = it * 256u + warp * 32u + lane;
+        for (int i = 0; i < 8; ++i) split_tf32x3_1(x[i], h[i], l[i]);
+        const uint32_t o0 = off_f32_chunk(row, 2 * g), o1 = off_f32_chunk(row, 2 * g + 1);
+        *reinterpret_cast<uint4*>(dst + o0) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(dst + o1) = make_uint4(h[4], h[5], h[6], h[7]);
+        *reinterpret_cast<uint4*>(dst + C::COMP_TILE + o0) = make_uint4(l[0], l[1], l[2], l[3]);
+        *reinterpret_cast<uint4*>(dst + C::COMP_TILE + o1) = make_uint4(l[4], l[5], l[6], l[7]);
+    }
+}
+
+// Split one operand half-tile (128 rows x 32 k) of a stage.  `src` is the
+// FP32 tile, `dst` the first component tile (components follow at COMP_TILE
+// strides).  `t` is the thread's index among NT split threads (NT a multiple
+// of 32).  Work items are (row, 8-k group) pairs, 512 per tile.
+template <int MODE, int NT>
+__device__ __forceinline__ void split_operand(const uint8_t* src, uint8_t* dst, bool mn_major, uint32_t t) {
+    if (!mn_major) {
+        // lanes cover 8 rows x 4 groups, so both the 16-byte reads and the
+        // 16-byte writes of a warp fall on distinct banks
+        for (uint32_t item = t; item < 512u; item += NT) {
             const uint32_t row = (item >> 5) * 8u + ((item & 31u) >> 2);
             const uint32_t g = item & 3u;
             const float4 lo4 = *reinterpret_cast<const float4*>(src + off_f32_chunk(row, 2 * g));
             const float4 hi4 = *reinterpret_cast<const float4*>(src + off_f32_chunk(row, 2 * g + 1));
             const float x[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
-            if constexpr (MODE == MODE_BF16X9) {
-                uint4 s0, s1, s2;
-                split_bf16x9_8(x, s0, s1, s2);
-                const uint32_t o = off_bf16_chunk(row, g);
-                *reinterpret_cast<uint4*>(dst + o) = s0;
-                *reinterpret_cast<uint4*>(dst + C::COMP_TILE + o) = s1;
-                *reinterpret_cast<uint4*>(dst + 2 * C::COMP_TILE + o) = s2;
-            } else {
-                uint32_t h[8], l[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) split_tf32x3_1(x[i], h[i], l[i]);
-                const uint32_t o0 = off_f32_chunk(row, 2 * g), o1 = off_f32_chunk(row, 2 * g + 1);
-                *reinterpret_cast<uint4*>(dst + o0) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4*>(dst + o1) = make_uint4(h[4], h[5], h[6], h[7]);
-                *reinterpret_cast<uint4*>(dst + C::COMP_TILE + o0) = make_uint4(l[0], l[1], l[2], l[3]);
-                *reinterpret_cast<uint4*>(dst + C::COMP_TILE + o1) = make_uint4(l[4], l[5], l[6], l[7]);
-            }
+            store_components<MODE>(dst, row, g, x);
         }
     } else {
-        // item = (mn, 8-k group): 32 consecutive mn per warp, so that both the
-        // column reads of the MN-major tile and the row writes are conflict-free
-#pragma unroll
-        for (int it = 0; it < 2; ++it) {
-            const uint32_t item = it * 256u + warp * 32u + lane;
+        // 32 consecutive mn per warp: the column reads of the MN-major tile and
+        // the row writes are both conflict-free
+        for (uint32_t item = t; item < 512u; item += NT) {
             const uint32_t mn = item & 127u;
             const uint32_t g = item >> 7;
             float x[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 x[i] = *reinterpret_cast<const float*>(src + off_f32_mnmajor(mn, 8 * g + i));
-            if constexpr (MODE == MODE_BF16X9) {
-                uint4 s0, s1, s2;
-                split_bf16x9_8(x, s0, s1, s2);
-                const uint32_t o = off_bf16_chunk(mn, g);
-                *reinterpret_cast<uint4*>(dst + o) = s0;
-                *reinterpret_cast<uint4*>(dst + C::COMP_TILE + o) = s1;
-                *reinterpret_cast<uint4*>(dst + 2 * C::COMP_TILE + o) = s2;
-            } else {
-                uint32_t h[8], l[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) split_tf32x3_1(x[i], h[i], l[i]);
-                const uint32_t o0 = off_f32_chunk(mn, 2 * g), o1 = off_f32_chunk(mn, 2 * g + 1);
-                *reinterpret_cast<uint4*>(dst + o0) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4*>(dst + o1) = make_uint4(h[4], h[5], h[6], h[7]);
-                *reinterpret_cast<uint4*>(dst + C::COMP_TILE + o0) = make_uint4(l[0], l[1], l[2], l[3]);
-                *reinterpret_cast<uint4*>(dst + C::COMP_TILE + o1) = make_uint4(l[4], l[5], l[6], l[7]);
-            }
+            store_components<MODE>(dst, mn, g, x);
         }
     }
 }
 
-// Issue the tensor-core products of one stage into TMEM accumulator `d`,
-// starting from zero.  BF16x9: bands 4, 3, 2, 1, 0 (i + j), each over the two
-// K=16 steps of the stage.  TF32x3: lo*hi, hi*lo, hi*hi over four K=8 steps.
+// Issue the pair products of one stage into TMEM accumulator `d`, starting
+// from zero.  BF16x9: bands 4, 3, 2, 1, 0 (i + j), each over the two K=16
+// steps of the stage.  TF32x3: lo*hi, hi*lo, hi*hi over four K=8 steps.
 template <int MODE>
 __device__ __forceinline__ void issue_stage_mmas(uint32_t d, uint32_t a_base, uint32_t b_base) {
     using C = Cfg<MODE>;
     uint32_t acc = 0;
     if constexpr (MODE == MODE_BF16X9) {
-        // (i, j) pairs, smallest band first
-        constexpr int PI[9] = {2, 1, 2, 0, 1, 2, 0, 1, 0};
+        constexpr int PI[9] = {2, 1, 2, 0, 1, 2, 0, 1, 0};  // (i, j), smallest band first
         constexpr int PJ[9] = {2, 2, 1, 2, 1, 0, 1, 0, 0};
 #pragma unroll
         for (int p = 0; p < 9; ++p) {
@@ -239,7 +240,7 @@ __device__ __forceinline__ void issue_stage_mmas(uint32_t d, uint32_t a_base, ui
             for (int ks = 0; ks < BK / 16; ++ks) {
                 const uint64_t ad = sdesc_kmajor(a_base + PI[p] * C::COMP_TILE + ks * 32, C::ROW_BYTES);
                 const uint64_t bd = sdesc_kmajor(b_base + PJ[p] * C::COMP_TILE + ks * 32, C::ROW_BYTES);
-                mma_bf16(d, ad, bd, C::IDESC, acc);
+                mma_bf16_pair(d, ad, bd, C::IDESC, acc);
                 acc = 1;
             }
         }
@@ -252,37 +253,57 @@ __device__ __forceinline__ void issue_stage_mmas(uint32_t d, uint32_t a_base, ui
             for (int ks = 0; ks < BK / 8; ++ks) {
                 const uint64_t ad = sdesc_kmajor(a_base + PI[p] * C::COMP_TILE + ks * 32, C::ROW_BYTES);
                 const uint64_t bd = sdesc_kmajor(b_base + PJ[p] * C::COMP_TILE + ks * 32, C::ROW_BYTES);
-                mma_tf32(d, ad, bd, C::IDESC, acc);
+                mma_tf32_pair(d, ad, bd, C::IDESC, acc);
                 acc = 1;
             }
         }
     }
 }
 
+struct Unit {
+    int tile, piece, kb, ke;
+};
+__device__ __forceinline__ Unit unit_of(const Params& p, int u) {
+    Unit w;
+    w.tile = u / p.split_k;
+    w.piece = u - w.tile * p.split_k;
+    w.kb = static_cast<int>((static_cast<long long>(w.piece) * p.k_stages) / p.split_k);
+    w.ke = static_cast<int>((static_cast<long long>(w.piece + 1) * p.k_stages) / p.split_k);
+    return w;
+}
+
 template <int MODE>
-__global__ void __launch_bounds__(NUM_THREADS, 1) emu_gemm_kernel(const __grid_constant__ Params p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+emu_gemm_kernel(const __grid_constant__ Params p) {
     using C = Cfg<MODE>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // pointer arithmetic on the shared array (not an integer round trip) keeps
+    // the shared address space visible to the compiler: shared stores then do
+    // not alias global loads, which it can hoist
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* fp32_ring = smem;
     uint8_t* slice_ring = smem + C::NF * FP32_STAGE_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(slice_ring + C::NS * C::SLICE_STAGE);
+    uint8_t* out_stage = slice_ring + C::NS * C::SLICE_STAGE;  // one 4 KB block per epilogue warp
+    uint64_t* bars = reinterpret_cast<uint64_t*>(out_stage + NUM_EPI_WARPS * STAGE_OUT_BYTES);
     uint64_t* fp32_full = bars;
     uint64_t* fp32_empty = fp32_full + C::NF;
-    uint64_t* slice_full = fp32_empty + C::NF;
-    uint64_t* slice_empty = slice_full + C::NS;
-    uint64_t* acc_full = slice_empty + C::NS;
-    uint64_t* acc_empty = acc_full + 2;
+    uint64_t* slice_full = fp32_empty + C::NF;   // leader: both CTAs' split warps
+    uint64_t* slice_empty = slice_full + C::NS;  // multicast commit
+    uint64_t* acc_full = slice_empty + C::NS;    // multicast commit
+    uint64_t* acc_empty = acc_full + 2;          // leader: both CTAs' epilogue warps
     uint64_t* drain = acc_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t cid = cluster_id_x(), ncl = num_clusters_x();
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::NF; ++s) { mbar_init(&fp32_full[s], 1); mbar_init(&fp32_empty[s], NUM_SPLIT_WARPS); }
-        for (int s = 0; s < C::NS; ++s) { mbar_init(&slice_full[s], NUM_SPLIT_WARPS); mbar_init(&slice_empty[s], 1); }
-        for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], NUM_EPI_WARPS); }
+        for (int s = 0; s < C::NF; ++s) { mbar_init(&fp32_full[s], 1); mbar_init(&fp32_empty[s], 1); }
+        for (int s = 0; s < C::NS; ++s) { mbar_init(&slice_full[s], 2); mbar_init(&slice_empty[s], 1); }
+        for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 2); }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -292,26 +313,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) emu_gemm_kernel(const __grid_c
         tma_prefetch_desc(&p.tmB);
     }
     if (warp == WARP_MMA) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // barriers of both CTAs initialised, TMEM of both allocated
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const uint64_t budget = p.wait_budget_ns;
 
     if (warp == WARP_PRODUCER) {
         // ------------------------------------------------------ producer ----
+        setmaxnreg_dec72();
         if (lane == 0) {
             int s = 0;
-            uint32_t ph = 0;
-            uint32_t issued_mask = 0;  // stages holding a load of the current lap
-            uint32_t issued_parity = 0;
+            uint32_t ph = 0, issued_mask = 0, issued_parity = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                const int m0 = (tile / p.tiles_n) * BM, n0 = (tile % p.tiles_n) * BN;
-                for (int ks = 0; ks < p.k_stages; ++ks) {
+            for (int u = cid; ok && u < p.num_units; u += ncl) {
+                const Unit w = unit_of(p, u);
+                const int m0 = (w.tile / p.tiles_n) * TILE_M + HALF * rank;
+                const int n0 = (w.tile % p.tiles_n) * TILE_N + HALF * rank;
+                for (int ks = w.kb; ks < w.ke; ++ks) {
                     if (!mbar_wait(&fp32_empty[s], ph ^ 1u, abort_flag, budget, 1)) { ok = false; break; }
                     uint64_t* full = &fp32_full[s];
                     mbar_arrive_expect_tx(full, FP32_STAGE_BYTES);
@@ -338,30 +360,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) emu_gemm_kernel(const __grid_c
         }
         __syncwarp();
     } else if (warp == WARP_MMA) {
-        // ---------------------------------------------------- MMA issuer ----
-        if (lane == 0) {
+        // ---------------------------------------------- MMA issuer (leader) -
+        setmaxnreg_dec72();
+        if (lane == 0 && rank == 0) {
             int s = 0, b = 0;
             uint32_t ph = 0, bph = 0;
             bool ok = true, issued = false;
             const uint32_t slice_base = smem_u32(slice_ring);
-            for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-                for (int ks = 0; ks < p.k_stages; ++ks) {
-                    if (!mbar_wait(&acc_empty[b], bph ^ 1u, abort_flag, budget, 2)) { ok = false; break; }
-                    if (!mbar_wait(&slice_full[s], ph, abort_flag, budget, 2)) { ok = false; break; }
+            for (int u = cid; ok && u < p.num_units; u += ncl) {
+                const Unit w = unit_of(p, u);
+                for (int ks = w.kb; ks < w.ke; ++ks) {
+                    if (!mbar_wait_cluster(&acc_empty[b], bph ^ 1u, abort_flag, budget, 2)) { ok = false; break; }
+                    if (!mbar_wait_cluster(&slice_full[s], ph, abort_flag, budget, 2)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_base = slice_base + s * C::SLICE_STAGE;
                     const uint32_t b_base = a_base + C::NCOMP * C::COMP_TILE;
-                    issue_stage_mmas<MODE>(tmem_base + b * BN, a_base, b_base);
+                    issue_stage_mmas<MODE>(tmem_base + b * TILE_N, a_base, b_base);
                     issued = true;
-                    mma_commit(&slice_empty[s]);
-                    mma_commit(&acc_full[b]);
+                    mma_commit_pair_multicast(&slice_empty[s], 0x3);
+                    mma_commit_pair_multicast(&acc_full[b], 0x3);
                     if (++s == C::NS) { s = 0; ph ^= 1u; }
                     if (++b == 2) { b = 0; bph ^= 1u; }
                 }
             }
             if (!ok && issued) {
                 // let the products in flight finish before TMEM is released
-                mma_commit(drain);
+                mma_commit_pair(drain);
                 volatile int never = 0;
                 mbar_wait(drain, 0, &never, 50000000ull, 2);
             }
@@ -369,23 +393,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) emu_gemm_kernel(const __grid_c
         __syncwarp();
     } else if (warp < WARP_EPI0) {
         // ---------------------------------------------------- split warps ---
+        setmaxnreg_dec72();
         const uint32_t t = threadIdx.x - WARP_SPLIT0 * 32;
         int fs = 0, ss = 0;
         uint32_t fph = 0, sph = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-            for (int ks = 0; ks < p.k_stages; ++ks) {
+        for (int u = cid; ok && u < p.num_units; u += ncl) {
+            const Unit w = unit_of(p, u);
+            for (int ks = w.kb; ks < w.ke; ++ks) {
                 if (!mbar_wait_warp(&fp32_full[fs], fph, abort_flag, budget, 3)) { ok = false; break; }
                 if (!mbar_wait_warp(&slice_empty[ss], sph ^ 1u, abort_flag, budget, 3)) { ok = false; break; }
                 const uint8_t* src = fp32_ring + fs * FP32_STAGE_BYTES;
                 uint8_t* dst = slice_ring + ss * C::SLICE_STAGE;
-                split_operand<MODE>(src, dst, p.a_mn_major != 0, t);
-                split_operand<MODE>(src + FP32_TILE_BYTES, dst + C::NCOMP * C::COMP_TILE, p.b_mn_major != 0, t);
+                split_operand<MODE, NUM_SPLIT_THREADS>(src, dst, p.a_mn_major != 0, t);
+                split_operand<MODE, NUM_SPLIT_THREADS>(src + FP32_TILE_BYTES, dst + C::NCOMP * C::COMP_TILE,
+                                                       p.b_mn_major != 0, t);
+                // one signal per CTA: the split threads meet, then a single
+                // thread releases the stage (a cluster-scope arrive is costly)
                 fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
+                named_bar_sync(SPLIT_BARRIER, NUM_SPLIT_THREADS);
+                if (t == 0) {
                     mbar_arrive(&fp32_empty[fs]);
-                    mbar_arrive(&slice_full[ss]);
+                    if (rank == 0) mbar_arrive(&slice_full[ss]);
+                    else mbar_arrive_cluster(&slice_full[ss], 0);
                 }
                 if (++fs == C::NF) { fs = 0; fph ^= 1u; }
                 if (++ss == C::NS) { ss = 0; sph ^= 1u; }
@@ -393,75 +423,160 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) emu_gemm_kernel(const __grid_c
         }
     } else {
         // ------------------------------------------------------- epilogue ---
-        const uint32_t e = warp - WARP_EPI0;
-        const uint32_t quarter = warp & 3u;      // TMEM lanes this warp may read
-        const uint32_t half = e >> 2;            // which 64 columns of the tile
+        setmaxnreg_inc184();
+        const uint32_t e = warp - WARP_EPI0;      // 0..7
+        const uint32_t quarter = warp & 3u;       // TMEM lanes this warp may read
+        const uint32_t half = e >> 2;             // which 128 columns of the tile
         const uint32_t lane_base = (quarter * 32u) << 16;
         int b = 0;
         uint32_t bph = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-            float acc[64];
+        for (int u = cid; ok && u < p.num_units; u += ncl) {
+            const Unit w = unit_of(p, u);
+            float acc[128];
 #pragma unroll
-            for (int i = 0; i < 64; ++i) acc[i] = 0.0f;
-            for (int ks = 0; ks < p.k_stages; ++ks) {
+            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+            for (int ks = w.kb; ks < w.ke; ++ks) {
                 if (!mbar_wait_warp(&acc_full[b], bph, abort_flag, budget, 4)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t col = tmem_base + b * BN + half * 64;
+                const uint32_t col = tmem_base + lane_base + b * TILE_N + half * 128;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float v[16];
-                    tmem_ld16(col + lane_base + c * 16, v);
+                for (int c = 0; c < 8; c += 2) {
+                    float v0[16], v1[16];
+                    tmem_ld16(col + c * 16, v0);
+                    tmem_ld16(col + (c + 1) * 16, v1);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[c * 16 + i] = __fadd_rn(acc[c * 16 + i], v[i]);
+                    for (int i = 0; i < 16; ++i) {
+                        acc[c * 16 + i] = __fadd_rn(acc[c * 16 + i], v0[i]);
+                        acc[(c + 1) * 16 + i] = __fadd_rn(acc[(c + 1) * 16 + i], v1[i]);
+                    }
                 }
                 tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[b]);
+                named_bar_sync(EPI_BARRIER, NUM_EPI_WARPS * 32);
+                if (e == 0 && lane == 0) {
+                    if (rank == 0) mbar_arrive(&acc_empty[b]);
+                    else mbar_arrive_cluster(&acc_empty[b], 0);
+                }
                 if (++b == 2) { b = 0; bph ^= 1u; }
             }
             if (!ok) break;
-            // C = alpha * acc + beta * C_old + bias
-            const int m0 = (tile / p.tiles_n) * BM, n0 = (tile % p.tiles_n) * BN;
-            const int row = m0 + static_cast<int>(quarter * 32u + lane);
-            const int col0 = n0 + static_cast<int>(half * 64u);
-            if (row < p.M) {
-                float* crow = p.c + static_cast<long long>(row) * p.ldc;
-                const float* orow = p.c_old + static_cast<long long>(row) * p.ldc;
+            const int row0 = (w.tile / p.tiles_n) * TILE_M + static_cast<int>(HALF * rank + quarter * 32u);
+            const int row = row0 + static_cast<int>(lane);
+            const int col0 = (w.tile % p.tiles_n) * TILE_N + static_cast<int>(half * 128u);
+            if (p.split_k > 1) {
+                // publish this piece's partial (thread-major: each warp store is
+                // 512 contiguous bytes); the last piece to arrive sums all pieces
+                const size_t per_piece = static_cast<size_t>(TILE_M) * TILE_N;
+                const size_t warp_off = (static_cast<size_t>(rank) * NUM_EPI_WARPS + e) * 4096u + lane * 4u;
+                float* part = p.workspace + (static_cast<size_t>(w.tile) * p.split_k + w.piece) * per_piece + warp_off;
 #pragma unroll
-                for (int j = 0; j < 64; j += 4) {
-                    const int col = col0 + j;
-                    if (col + 3 < p.N) {
-                        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (p.beta != 0.0f) o = *reinterpret_cast<const float4*>(orow + col);
-                        float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (p.bias) bb = *reinterpret_cast<const float4*>(p.bias + col);
-                        float4 r;
-                        r.x = __fadd_rn(__fmaf_rn(p.alpha, acc[j + 0], p.beta != 0.0f ? __fmul_rn(p.beta, o.x) : 0.0f), bb.x);
-                        r.y = __fadd_rn(__fmaf_rn(p.alpha, acc[j + 1], p.beta != 0.0f ? __fmul_rn(p.beta, o.y) : 0.0f), bb.y);
-                        r.z = __fadd_rn(__fmaf_rn(p.alpha, acc[j + 2], p.beta != 0.0f ? __fmul_rn(p.beta, o.z) : 0.0f), bb.z);
-                        r.w = __fadd_rn(__fmaf_rn(p.alpha, acc[j + 3], p.beta != 0.0f ? __fmul_rn(p.beta, o.w) : 0.0f), bb.w);
-                        *reinterpret_cast<float4*>(crow + col) = r;
-                    } else {
+                for (int j = 0; j < 32; ++j)
+                    __stcg(reinterpret_cast<float4*>(part + j * 128),
+                           make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
+                __threadfence();
+                named_bar_sync(EPI_BARRIER, NUM_EPI_WARPS * 32);
+                if (e == 0 && lane == 0) {
+                    int* ctr = p.counters + w.tile * 2 + rank;
+                    const int prev = atomicAdd(ctr, 1);
+                    const int last = prev == p.split_k - 1;
+                    if (last) atomicExch(ctr, 0);  // ready for the next launch
+                    *last_flag = last;
+                }
+                named_bar_sync(EPI_BARRIER, NUM_EPI_WARPS * 32);
+                const int is_last = *last_flag;
+                named_bar_sync(EPI_BARRIER, NUM_EPI_WARPS * 32);  // flag read before the next unit rewrites it
+                if (!is_last) continue;
+                __threadfence();
+                // fixed order 0, 1, ..., S-1, whichever piece arrived last
+                const float* part0 = p.workspace + static_cast<size_t>(w.tile) * p.split_k * per_piece + warp_off;
+                // (eight float4 loads in flight at a time keeps the registers in budget)
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            if (col + q < p.N) {
-                                const float bc = p.beta != 0.0f ? __fmul_rn(p.beta, orow[col + q]) : 0.0f;
-                                const float bi = p.bias ? p.bias[col + q] : 0.0f;
-                                crow[col + q] = __fadd_rn(__fmaf_rn(p.alpha, acc[j + q], bc), bi);
-                            }
+                for (int jj = 0; jj < 32; jj += 8)
+                for (int q = 0; q < p.split_k; ++q) {
+#pragma unroll
+                    for (int j = jj; j < jj + 8; ++j) {
+                        const float4 v = __ldcg(reinterpret_cast<const float4*>(part0 + q * per_piece + j * 128));
+                        if (q == 0) {
+                            acc[4 * j] = v.x; acc[4 * j + 1] = v.y; acc[4 * j + 2] = v.z; acc[4 * j + 3] = v.w;
+                        } else {
+                            acc[4 * j] = __fadd_rn(acc[4 * j], v.x);
+                            acc[4 * j + 1] = __fadd_rn(acc[4 * j + 1], v.y);
+                            acc[4 * j + 2] = __fadd_rn(acc[4 * j + 2], v.z);
+                            acc[4 * j + 3] = __fadd_rn(acc[4 * j + 3], v.w);
                         }
                     }
                 }
+            }
+            // 4 blocks of 32 x 32: each lane stages its row's 32 sums in shared
+            // memory (128-byte rows, 128-byte swizzle); the warp then reads them
+            // back as 4 whole row segments per pass, applies
+            // C = alpha * acc + beta * C_old + bias and stores 128 contiguous
+            // bytes per row (coalesced), clipping rows and columns outside C.
+            uint8_t* stage = out_stage + e * STAGE_OUT_BYTES;
+            const float alpha = p.alpha, beta = p.beta;
+            const uint32_t q = lane & 7u;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<float4*>(stage + off_f32_chunk(lane, j)) =
+                        make_float4(acc[32 * c + 4 * j], acc[32 * c + 4 * j + 1], acc[32 * c + 4 * j + 2],
+                                    acc[32 * c + 4 * j + 3]);
+                __syncwarp();
+                const int gcol = col0 + 32 * c + static_cast<int>(4 * q);  // this lane's 4 columns
+                const bool full4 = gcol + 3 < p.N;
+                float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (p.bias) {
+                    if (full4) {
+                        bb = __ldg(reinterpret_cast<const float4*>(p.bias + gcol));
+                    } else {
+                        if (gcol + 0 < p.N) bb.x = __ldg(p.bias + gcol + 0);
+                        if (gcol + 1 < p.N) bb.y = __ldg(p.bias + gcol + 1);
+                        if (gcol + 2 < p.N) bb.z = __ldg(p.bias + gcol + 2);
+                    }
+                }
+#pragma unroll
+                for (int pass = 0; pass < 8; ++pass) {
+                    const uint32_t rr = pass * 4u + (lane >> 3);
+                    const float4 v = *reinterpret_cast<const float4*>(stage + off_f32_chunk(rr, q));
+                    const int grow = row0 + static_cast<int>(rr);
+                    if (grow >= p.M) continue;
+                    float* dst = p.c + static_cast<long long>(grow) * p.ldc + gcol;
+                    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (beta != 0.0f) {
+                        const float* src_old = p.c_old + static_cast<long long>(grow) * p.ldc + gcol;
+                        if (full4) {
+                            o = *reinterpret_cast<const float4*>(src_old);
+                        } else {
+                            if (gcol + 0 < p.N) o.x = src_old[0];
+                            if (gcol + 1 < p.N) o.y = src_old[1];
+                            if (gcol + 2 < p.N) o.z = src_old[2];
+                        }
+                        o = make_float4(__fmul_rn(beta, o.x), __fmul_rn(beta, o.y), __fmul_rn(beta, o.z),
+                                        __fmul_rn(beta, o.w));
+                    }
+                    const float4 r = make_float4(__fadd_rn(__fmaf_rn(alpha, v.x, o.x), bb.x),
+                                                 __fadd_rn(__fmaf_rn(alpha, v.y, o.y), bb.y),
+                                                 __fadd_rn(__fmaf_rn(alpha, v.z, o.z), bb.z),
+                                                 __fadd_rn(__fmaf_rn(alpha, v.w, o.w), bb.w));
+                    if (full4) {
+                        *reinterpret_cast<float4*>(dst) = r;
+                    } else {
+                        if (gcol + 0 < p.N) dst[0] = r.x;
+                        if (gcol + 1 < p.N) dst[1] = r.y;
+                        if (gcol + 2 < p.N) dst[2] = r.z;
+                    }
+                }
+                __syncwarp();  // staging buffer free for the next block
             }
         }
     }
 
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // no CTA leaves while its peer may still use its TMEM or barriers
     tc_fence_after();
-    if (warp == WARP_MMA) tmem_dealloc(tmem_base, TMEM_COLS);
+    if (warp == WARP_MMA) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 }  // namespace emu

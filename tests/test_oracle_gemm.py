@@ -193,6 +193,21 @@ def test_tf32x3_gemm_against_exact_rationals(tA, tB):
         assert err <= 3 * K * U + 3 * 2.0 ** -22
 
 
+def test_tf32x3_single_product_error_floor():
+    """K = 1: the method's own error (lo*lo dropped, split residuals) reaches
+    beyond 4u but stays below 2^-21 = 8u, which is why the TF32x3 normwise
+    bound reads K as max(K, 2); BF16x9 at K = 1 stays near one rounding."""
+    rng = np.random.default_rng(20)
+    a = _bits.random_bits_matrix(rng, (4000, 1), -10, 10)
+    b = _bits.random_bits_matrix(rng, (1, 50), -10, 10)
+    exact = a.astype(np.float64) @ b.astype(np.float64)  # exact: 48-bit products
+    rel_tf = np.abs(oracle.gemm_tf32x3(oracle.Problem(a, b)) - exact) / np.abs(exact)
+    rel_bf = np.abs(oracle.gemm_bf16x9(oracle.Problem(a, b)) - exact) / np.abs(exact)
+    assert rel_tf.max() > 4 * U and rel_tf.max() <= 8 * U
+    assert rel_tf.max() <= oracle.normwise_bound("tf32x3", 1)
+    assert rel_bf.max() <= oracle.normwise_bound("bf16x9", 1)
+
+
 # ------------------------------------------- closed forms (all variants) ----
 def _all_modes(p):
     return {
