@@ -42,6 +42,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-comparators", action="store_true")
     return ap.parse_args()
 
 
@@ -314,16 +315,68 @@ def main():
         line["e2e"] = e2e
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(s, args.mode)
+    if not args.no_comparators:
+        line["comparators"] = cublas_comparators(s)
     print(json.dumps(line), flush=True)
+
+
+def cublas_comparators(shape, steps=200):
+    """Same step through torch.matmul on the same GPU: native FP32 SGEMM
+    (TF32 off) and cuBLAS's own BF16x9 path (CUBLAS_EMULATE_SINGLE_PRECISION=1,
+    set before cuBLAS loads, so it runs in a child process).  Context only."""
+    out = {}
+    code = r"""
+import json, os, sys, torch
+M, K, N, steps = %d, %d, %d, %d
+torch.backends.cuda.matmul.allow_tf32 = False
+dev = torch.device('cuda')
+X = torch.randn(M, K, device=dev); W = torch.randn(N, K, device=dev) / K ** 0.5
+b = torch.randn(N, device=dev) * 0.1; dY = torch.randn(M, N, device=dev)
+flush = torch.empty(64 * 1024 * 1024, device=dev)
+def step():
+    torch.addmm(b, X, W.t()); dY.mm(W)
+for _ in range(10): step()
+torch.cuda.synchronize()
+tot = 0.0
+for _ in range(steps):
+    flush.fill_(1.0)
+    e0 = torch.cuda.Event(enable_timing=True); e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(); step(); e1.record(); torch.cuda.synchronize(); tot += e0.elapsed_time(e1)
+print(json.dumps({"ms": tot / steps}))
+""" % (shape.M, shape.K, shape.N, steps)
+    for name, env in (("cublas_sgemm_native", {}), ("cublas_bf16x9_emulated", {"CUBLAS_EMULATE_SINGLE_PRECISION": "1"})):
+        try:
+            r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300,
+                               env=dict(os.environ, **env))
+            ms = json.loads(r.stdout.strip().splitlines()[-1])["ms"]
+            out[name] = {"value": step_flops(shape) / (ms * 1e-3) / 1e12, "unit": "TFLOPS", "ms_per_step": ms}
+        except Exception as exc:  # reported, not fatal
+            out[name] = {"unavailable": str(exc)[:200]}
+    return out
+
+
+def kernel_source_hash():
+    """sha256 over the CUDA sources of the library (what an ncu capture measured)."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp32_emulated_gemm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
 
 
 def load_traffic(args):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary for this workload, or None when no capture matches the kernel."""
+    summary for this workload, or None when no capture exists or the kernel
+    sources changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", f"traffic_{args.workload}_{args.mode}.json")
     try:
         with open(path) as f:
             d = json.load(f)
+        if d.get("kernel_source_sha256") != kernel_source_hash():
+            return None
         return d.get("dram_bytes_per_launch")
     except Exception:
         return None
