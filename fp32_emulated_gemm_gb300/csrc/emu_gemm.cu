@@ -429,3 +429,4 @@ emu_status_t emu_split_dump(emu_mode_t mode, int64_t R, int64_t Kc, const float*
 int emu_version(void) { return 100; }
 
 }  // extern "C"
+

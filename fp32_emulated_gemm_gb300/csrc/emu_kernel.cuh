@@ -462,7 +462,6 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
             }
             if (!ok) break;
             const int row0 = (w.tile / p.tiles_n) * TILE_M + static_cast<int>(HALF * rank + quarter * 32u);
-            const int row = row0 + static_cast<int>(lane);
             const int col0 = (w.tile % p.tiles_n) * TILE_N + static_cast<int>(half * 128u);
             if (p.split_k > 1) {
                 // publish this piece's partial (thread-major: each warp store is

@@ -23,8 +23,11 @@
  *     of an R x C matrix X with leading dimension ldx is X[i * ldx + j].
  *   - op(X) = X when the op is EMU_OP_N, X^T when it is EMU_OP_T.
  *   - Pointers: caller-owned DEVICE memory of the current CUDA device.  The
- *     library allocates nothing on the device and keeps no pointer after the
- *     call returns; it never frees caller memory.
+ *     library keeps no caller pointer after the call returns and never frees
+ *     caller memory.  Its only device allocation is a split-K workspace
+ *     (partial tiles for problems with few tiles), made with cudaMallocAsync
+ *     on first need per (device, stream) and kept until the process exits;
+ *     emu_sgemm_noalloc never allocates.
  *   - Alignment (TMA): A and B must start on a 16-byte boundary and lda, ldb
  *     must be multiples of 4 elements; C the same (ldc multiple of 4).
  *     Violations return EMU_STATUS_NOT_SUPPORTED.
@@ -69,9 +72,9 @@ typedef enum { EMU_OP_N = 0, EMU_OP_T = 1 } emu_op_t;
 typedef enum {
     EMU_STATUS_SUCCESS = 0,
     EMU_STATUS_INVALID_VALUE = 1,   /* negative size, ld too small, NULL with non-zero size, bad enum */
-    EMU_STATUS_NOT_SUPPORTED = 2,   /* pointer or leading dimension not aligned for TMA */
+    EMU_STATUS_NOT_SUPPORTED = 2,   /* pointer or leading dimension not aligned for TMA; size too large */
     EMU_STATUS_ARCH_MISMATCH = 3,   /* current device is not compute capability 10.x (sm_100 family) */
-    EMU_STATUS_ALLOC_FAILED = 4,    /* reserved: the library does not allocate device memory */
+    EMU_STATUS_ALLOC_FAILED = 4,    /* the split-K workspace could not be allocated */
     EMU_STATUS_LAUNCH_FAILED = 5,   /* a CUDA call failed (no device, launch error, TMA encode error) */
     EMU_STATUS_DEVICE_TIMEOUT = 6   /* a kernel gave up on an internal wait and returned early */
 } emu_status_t;
