@@ -430,3 +430,127 @@ int emu_version(void) { return 100; }
 
 }  // extern "C"
 
+// ---------------------------------------------------------------------------
+// emu_sgemm_noalloc: the same GEMM for callers that cannot allocate device
+// memory (see include/emu_gemm.h).  Its split-K scratch is a file-scope
+// device array instead of a cudaMallocAsync'd workspace; everything else
+// (checks, plan, kernel) is what emu_sgemm does.
+// ---------------------------------------------------------------------------
+namespace emu {
+
+// 64 MiB, held by every device that loads this library until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+// Device address of g_noalloc_scratch for the current device, looked up once
+// per device (cudaGetSymbolAddress, not an allocation).  In host code the
+// array's name is only a stand-in for the symbol; kernels must get this
+// address, never the name's host-side value.
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+emu_status_t noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return EMU_STATUS_LAUNCH_FAILED;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+            cudaGetLastError();
+            return EMU_STATUS_LAUNCH_FAILED;
+        }
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return EMU_STATUS_SUCCESS;
+}
+
+emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t N, int64_t K,
+                              float alpha, const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
+                              float* C, int64_t ldc, cudaStream_t stream) {
+    if (mode != EMU_MODE_BF16X9 && mode != EMU_MODE_TF32X3) return EMU_STATUS_INVALID_VALUE;
+    if (M < 0 || N < 0 || K < 0) return EMU_STATUS_INVALID_VALUE;
+    if (M > INT32_MAX - 256 || N > INT32_MAX - 256 || K > INT32_MAX - 256) return EMU_STATUS_NOT_SUPPORTED;
+    if (M == 0 || N == 0) return EMU_STATUS_SUCCESS;
+    const int64_t a_cols = a_mn ? M : K, b_cols = b_mn ? N : K;
+    if (ldc < N || !C) return EMU_STATUS_INVALID_VALUE;
+    const bool gemm = K > 0 && alpha != 0.0f;
+    if (gemm) {
+        if (!A || !B || lda < a_cols || ldb < b_cols) return EMU_STATUS_INVALID_VALUE;
+        if (!aligned16(A) || !aligned16(B) || (lda & 3) || (ldb & 3)) return EMU_STATUS_NOT_SUPPORTED;
+    }
+    if (!aligned16(C) || (ldc & 3)) return EMU_STATUS_NOT_SUPPORTED;
+
+    DeviceInfo* dev = nullptr;
+    emu_status_t st = device_info(&dev);
+    if (st != EMU_STATUS_SUCCESS) return st;
+    void* scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != EMU_STATUS_SUCCESS) return st;
+
+    if (!gemm) {
+        const int64_t total = M * N;
+        const int threads = 256;
+        const int64_t blocks64 = (total + threads - 1) / threads;
+        const int blocks = (int)(blocks64 < dev->sm_count * 8 ? blocks64 : dev->sm_count * 8);
+        scale_kernel<<<blocks, threads, 0, stream>>>(M, N, beta, C, ldc, nullptr);
+        return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
+    }
+
+    Params p{};
+    if (!encode_operand(&p.tmA, A, a_mn, M, K, lda) || !encode_operand(&p.tmB, B, b_mn, N, K, ldb))
+        return EMU_STATUS_LAUNCH_FAILED;
+    p.M = (int)M; p.N = (int)N; p.K = (int)K;
+    p.a_mn_major = a_mn; p.b_mn_major = b_mn;
+    p.tiles_m = (int)((M + TILE_M - 1) / TILE_M);
+    p.tiles_n = (int)((N + TILE_N - 1) / TILE_N);
+    p.num_tiles = p.tiles_m * p.tiles_n;
+    p.k_stages = (int)((K + BK - 1) / BK);
+    const int pairs = dev->max_clusters[mode == EMU_MODE_BF16X9 ? 0 : 1];
+    p.split_k = choose_split_k(p.num_tiles, p.k_stages, pairs);
+    p.num_units = p.num_tiles * p.split_k;
+    p.alpha = alpha; p.beta = beta;
+    p.c_old = C; p.c = C; p.ldc = ldc;
+    p.bias = nullptr;
+    p.wait_budget_ns = wait_budget_ns();
+    if (p.split_k > 1) {
+        // partial tiles first, then one counter per CTA half-tile
+        const size_t partial_bytes = (size_t)p.num_tiles * p.split_k * TILE_M * TILE_N * sizeof(float);
+        const size_t counter_off = (partial_bytes + 255) & ~size_t(255);
+        const size_t counter_bytes = (size_t)p.num_tiles * 2 * sizeof(int);
+        if (counter_off + counter_bytes > kNoAllocScratchBytes) return EMU_STATUS_NOT_SUPPORTED;
+        p.workspace = reinterpret_cast<float*>(scratch);
+        p.counters = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(scratch) + counter_off);
+        // the array keeps the previous call's contents: the counters must start at zero
+        if (cudaMemsetAsync(p.counters, 0, counter_bytes, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return EMU_STATUS_LAUNCH_FAILED;
+        }
+    }
+    const int clusters = p.num_units < pairs ? p.num_units : pairs;
+    const dim3 grid(2 * clusters, 1, 1);
+    if (mode == EMU_MODE_BF16X9)
+        emu_gemm_kernel<MODE_BF16X9><<<grid, NUM_THREADS, smem_bytes<MODE_BF16X9>(), stream>>>(p);
+    else
+        emu_gemm_kernel<MODE_TF32X3><<<grid, NUM_THREADS, smem_bytes<MODE_TF32X3>(), stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
+}
+
+}  // namespace
+}  // namespace emu
+
+extern "C" emu_status_t emu_sgemm_noalloc(emu_mode_t mode, emu_op_t transA, emu_op_t transB, int64_t M,
+                                          int64_t N, int64_t K, float alpha, const float* A, int64_t lda,
+                                          const float* B, int64_t ldb, float beta, float* C, int64_t ldc,
+                                          emu_stream_t stream) {
+    using namespace emu;
+    if ((transA != EMU_OP_N && transA != EMU_OP_T) || (transB != EMU_OP_N && transB != EMU_OP_T))
+        return EMU_STATUS_INVALID_VALUE;
+    return run_gemm_noalloc(mode, transA == EMU_OP_T, transB == EMU_OP_N, M, N, K, alpha, A, lda, B, ldb, beta, C,
+                            ldc, reinterpret_cast<cudaStream_t>(stream));
+}

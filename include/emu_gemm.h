@@ -144,6 +144,45 @@ emu_status_t emu_stream_check(emu_stream_t stream);
 emu_status_t emu_split_dump(emu_mode_t mode, int64_t R, int64_t Kc, const float *X, int64_t ldx,
                             int mn_major, void *out, emu_stream_t stream);
 
+/*
+ * emu_sgemm_noalloc -- emu_sgemm for callers that cannot allocate device
+ * memory: applications that hand all device memory to their own pre-sized
+ * pool or allocator and forbid driver allocations behind its back,
+ * latency-critical loops that must not enter the driver's allocator (which
+ * can block or synchronise), and callers that must never fail with an
+ * out-of-memory error in the middle of a run.  The blog has no counterpart;
+ * this is an engineering entry point of this library.
+ *
+ * Same arguments, same plan and same kernel as emu_sgemm (results are the
+ * same bits).  The only device memory emu_sgemm may allocate is the split-K
+ * scratch (partial tiles and counters for problems with few tiles); here it
+ * lives in a fixed 64 MiB device array inside the library instead.  The
+ * array is reserved on every GPU that loads the library and kept until the
+ * process exits.
+ *   - Size limit: a plan that splits K into S pieces needs
+ *     tiles * S * 256 KiB (+ 8 bytes per tile, tiles = ceil(M/256) *
+ *     ceil(N/256)); if that exceeds 64 MiB the call returns
+ *     EMU_STATUS_NOT_SUPPORTED and enqueues nothing.  Plans without a split
+ *     use no scratch and are never rejected for size.
+ *   - Allocation: none (no cudaMalloc/cudaFree, no allocating library
+ *     routine).  The call enqueues one cudaMemsetAsync of the counters (the
+ *     array keeps the previous call's contents; the counters must start at
+ *     zero) and the kernel.
+ *   - First call per device: looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make this first call
+ *     before any stream capture.
+ *   - Concurrency: every call on a device shares the one array, so calls
+ *     whose executions overlap on the GPU (different streams, or concurrent
+ *     graph branches) race and corrupt each other's split-K partials;
+ *     serialise them (one stream, or events).
+ * Errors as for emu_sgemm.
+ */
+emu_status_t emu_sgemm_noalloc(emu_mode_t mode, emu_op_t transA, emu_op_t transB,
+                               int64_t M, int64_t N, int64_t K,
+                               float alpha, const float *A, int64_t lda,
+                               const float *B, int64_t ldb,
+                               float beta, float *C, int64_t ldc, emu_stream_t stream);
+
 /* Library version as an integer (major * 10000 + minor * 100 + patch). */
 int emu_version(void);
 
