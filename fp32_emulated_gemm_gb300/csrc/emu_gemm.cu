@@ -28,7 +28,7 @@ struct DeviceInfo {
     bool ready = false;
     int cc_major = 0, cc_minor = 0, sm_count = 0;
     bool attrs_set = false;
-    int max_clusters[2] = {0, 0};  // co-resident CTA pairs per mode
+    int max_clusters[2] = {0, 0};  // co-resident CTA pairs per mode (all pipeline shapes)
 };
 
 // Split-K workspace: partial tiles plus per-tile counters, owned by the
@@ -79,23 +79,30 @@ emu_status_t device_info(DeviceInfo** out) {
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     if (!d.attrs_set) {
-        if (cudaFuncSetAttribute(emu_gemm_kernel<MODE_BF16X9>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_bytes<MODE_BF16X9>()) != cudaSuccess ||
-            cudaFuncSetAttribute(emu_gemm_kernel<MODE_TF32X3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_bytes<MODE_TF32X3>()) != cudaSuccess) {
+        if (cudaFuncSetAttribute(emu_gemm_kernel<MODE_BF16X9, PIPE_SHORT_K>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_bytes<MODE_BF16X9, PIPE_SHORT_K>()) != cudaSuccess ||
+            cudaFuncSetAttribute(emu_gemm_kernel<MODE_BF16X9, PIPE_LONG_K>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_bytes<MODE_BF16X9, PIPE_LONG_K>()) != cudaSuccess ||
+            cudaFuncSetAttribute(emu_gemm_kernel<MODE_TF32X3, PIPE_SHORT_K>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_bytes<MODE_TF32X3, PIPE_SHORT_K>()) != cudaSuccess) {
             cudaGetLastError();
             return EMU_STATUS_LAUNCH_FAILED;
         }
-        // how many CTA pairs can be resident at once (the persistent grid)
+        // how many CTA pairs can be resident at once (the persistent grid);
+        // every shape uses one CTA per SM, so the smallest count serves all
         for (int m = 0; m < 2; ++m) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(2 * (d.sm_count / 2), 1, 1);
             cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-            cfg.dynamicSmemBytes = m == 0 ? smem_bytes<MODE_BF16X9>() : smem_bytes<MODE_TF32X3>();
+            cfg.dynamicSmemBytes = m == 0 ? smem_bytes<MODE_BF16X9, PIPE_SHORT_K>()
+                                          : smem_bytes<MODE_TF32X3, PIPE_SHORT_K>();
             int n = 0;
             const cudaError_t e = m == 0
-                ? cudaOccupancyMaxActiveClusters(&n, emu_gemm_kernel<MODE_BF16X9>, &cfg)
-                : cudaOccupancyMaxActiveClusters(&n, emu_gemm_kernel<MODE_TF32X3>, &cfg);
+                ? cudaOccupancyMaxActiveClusters(&n, emu_gemm_kernel<MODE_BF16X9, PIPE_SHORT_K>, &cfg)
+                : cudaOccupancyMaxActiveClusters(&n, emu_gemm_kernel<MODE_TF32X3, PIPE_SHORT_K>, &cfg);
             if (e != cudaSuccess || n <= 0) {
                 cudaGetLastError();
                 n = d.sm_count / 2;
@@ -235,6 +242,25 @@ unsigned long long wait_budget_ns() {
     return v;
 }
 
+// Long k-loops per work unit favour three component stages; short ones the
+// wider output staging (see PipeCfg).
+constexpr int kLongKMinStages = 16;
+
+cudaError_t launch_gemm(emu_mode_t mode, const Params& p, int clusters, cudaStream_t stream) {
+    const dim3 grid(2 * clusters, 1, 1);
+    const int per_unit = (p.k_stages + p.split_k - 1) / p.split_k;
+    if (mode == EMU_MODE_TF32X3)
+        emu_gemm_kernel<MODE_TF32X3, PIPE_SHORT_K>
+            <<<grid, NUM_THREADS, smem_bytes<MODE_TF32X3, PIPE_SHORT_K>(), stream>>>(p);
+    else if (per_unit >= kLongKMinStages)
+        emu_gemm_kernel<MODE_BF16X9, PIPE_LONG_K>
+            <<<grid, NUM_THREADS, smem_bytes<MODE_BF16X9, PIPE_LONG_K>(), stream>>>(p);
+    else
+        emu_gemm_kernel<MODE_BF16X9, PIPE_SHORT_K>
+            <<<grid, NUM_THREADS, smem_bytes<MODE_BF16X9, PIPE_SHORT_K>(), stream>>>(p);
+    return cudaGetLastError();
+}
+
 // Core: C = alpha * op(A) op(B) + beta * C_old + bias, with C_old == C.
 emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t N, int64_t K, float alpha,
                       const float* A, int64_t lda, const float* B, int64_t ldb, float beta, float* C,
@@ -295,18 +321,13 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
         p.counters = w->counters;
     }
     const int clusters = p.num_units < pairs ? p.num_units : pairs;
-    const dim3 grid(2 * clusters, 1, 1);
     if (log_enabled())
         std::fprintf(stderr, "[emu] %s M=%lld N=%lld K=%lld a_mn=%d b_mn=%d tiles=%dx%d k_stages=%d split_k=%d "
-                             "units=%d pairs=%d (max %d) smem=%u\n",
+                             "units=%d pairs=%d (max %d) long_k_pipe=%u\n",
                      mode == EMU_MODE_BF16X9 ? "bf16x9" : "tf32x3", (long long)M, (long long)N, (long long)K,
                      (int)a_mn, (int)b_mn, p.tiles_m, p.tiles_n, p.k_stages, p.split_k, p.num_units, clusters,
-                     pairs, mode == EMU_MODE_BF16X9 ? smem_bytes<MODE_BF16X9>() : smem_bytes<MODE_TF32X3>());
-    if (mode == EMU_MODE_BF16X9)
-        emu_gemm_kernel<MODE_BF16X9><<<grid, NUM_THREADS, smem_bytes<MODE_BF16X9>(), stream>>>(p);
-    else
-        emu_gemm_kernel<MODE_TF32X3><<<grid, NUM_THREADS, smem_bytes<MODE_TF32X3>(), stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
+                     pairs, (p.k_stages + p.split_k - 1) / p.split_k >= kLongKMinStages ? 1u : 0u);
+    return launch_gemm(mode, p, clusters, stream) == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
 }
 
 // ----------------------------------------------------------- split dump ----
@@ -533,12 +554,7 @@ emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, 
         }
     }
     const int clusters = p.num_units < pairs ? p.num_units : pairs;
-    const dim3 grid(2 * clusters, 1, 1);
-    if (mode == EMU_MODE_BF16X9)
-        emu_gemm_kernel<MODE_BF16X9><<<grid, NUM_THREADS, smem_bytes<MODE_BF16X9>(), stream>>>(p);
-    else
-        emu_gemm_kernel<MODE_TF32X3><<<grid, NUM_THREADS, smem_bytes<MODE_TF32X3>(), stream>>>(p);
-    return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
+    return launch_gemm(mode, p, clusters, stream) == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
 }
 
 }  // namespace

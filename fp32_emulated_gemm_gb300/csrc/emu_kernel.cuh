@@ -63,7 +63,6 @@ constexpr int NUM_EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 2 * TILE_N;  // two accumulators, double-buffered (all 512)
 constexpr uint32_t EPI_BARRIER = 1;         // named barrier of the 256 epilogue threads
 constexpr uint32_t SPLIT_BARRIER = 2;       // named barrier of the split threads
-constexpr uint32_t STAGE_OUT_BYTES = 32 * 32 * 4;  // one epilogue warp's 32 x 32 output block
 
 // FP32 stage of one CTA: its op(A) half-tile then its op(B) half-tile.
 constexpr uint32_t FP32_TILE_BYTES = HALF * BK * 4;           // 16 KB
@@ -75,8 +74,6 @@ template <> struct Cfg<MODE_BF16X9> {
     static constexpr uint32_t ROW_BYTES = BK * 2;    // 64: one BF16 row of a stage
     static constexpr uint32_t COMP_TILE = HALF * ROW_BYTES;         // 8 KB
     static constexpr uint32_t SLICE_STAGE = 2 * NCOMP * COMP_TILE;  // 48 KB
-    static constexpr int NF = 3;                     // FP32 stages
-    static constexpr int NS = 2;                     // component stages
     static constexpr uint32_t IDESC = make_idesc(1, TILE_M, TILE_N);
 };
 template <> struct Cfg<MODE_TF32X3> {
@@ -84,15 +81,32 @@ template <> struct Cfg<MODE_TF32X3> {
     static constexpr uint32_t ROW_BYTES = BK * 4;    // 128
     static constexpr uint32_t COMP_TILE = HALF * ROW_BYTES;         // 16 KB
     static constexpr uint32_t SLICE_STAGE = 2 * NCOMP * COMP_TILE;  // 64 KB
-    static constexpr int NF = 2;
-    static constexpr int NS = 2;
     static constexpr uint32_t IDESC = make_idesc(2, TILE_M, TILE_N);
 };
 
-template <int MODE>
+// Pipeline depths and output staging, chosen per launch.  Shared memory
+// cannot hold both deep rings and wide staging blocks, so there are two
+// shapes: PIPE_SHORT_K (more FP32 stages, 32-column staging blocks: fastest
+// when a work unit has few k-stages and the output stores come often) and
+// PIPE_LONG_K (three component stages, 16-column blocks: fastest in long
+// k-loops).  TF32x3's larger components leave room for only one shape.
+enum Pipe : int { PIPE_SHORT_K = 0, PIPE_LONG_K = 1 };
+template <int MODE, int PIPE> struct PipeCfg;
+template <> struct PipeCfg<MODE_BF16X9, PIPE_SHORT_K> {
+    static constexpr int NF = 3, NS = 2, OUT_COLS = 32;
+};
+template <> struct PipeCfg<MODE_BF16X9, PIPE_LONG_K> {
+    static constexpr int NF = 2, NS = 3, OUT_COLS = 16;
+};
+template <int PIPE> struct PipeCfg<MODE_TF32X3, PIPE> {
+    static constexpr int NF = 2, NS = 2, OUT_COLS = 32;
+};
+
+template <int MODE, int PIPE>
 constexpr uint32_t smem_bytes() {
-    return 1024 /* alignment slack */ + Cfg<MODE>::NF * FP32_STAGE_BYTES + Cfg<MODE>::NS * Cfg<MODE>::SLICE_STAGE +
-           NUM_EPI_WARPS * STAGE_OUT_BYTES + 1024 /* barriers and flags */;
+    using P = PipeCfg<MODE, PIPE>;
+    return 1024 /* alignment slack */ + P::NF * FP32_STAGE_BYTES + P::NS * Cfg<MODE>::SLICE_STAGE +
+           NUM_EPI_WARPS * (32 * P::OUT_COLS * 4) + 1024 /* barriers and flags */;
 }
 
 struct Params {
@@ -272,24 +286,27 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int u) {
     return w;
 }
 
-template <int MODE>
+template <int MODE, int PIPE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 emu_gemm_kernel(const __grid_constant__ Params p) {
     using C = Cfg<MODE>;
+    using PC = PipeCfg<MODE, PIPE>;
+    constexpr int NF = PC::NF, NS = PC::NS, OUT_COLS = PC::OUT_COLS;
+    constexpr uint32_t STAGE_OUT_BYTES = 32 * OUT_COLS * 4;  // one epilogue warp's 32 x OUT_COLS block
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // pointer arithmetic on the shared array (not an integer round trip) keeps
     // the shared address space visible to the compiler: shared stores then do
     // not alias global loads, which it can hoist
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* fp32_ring = smem;
-    uint8_t* slice_ring = smem + C::NF * FP32_STAGE_BYTES;
-    uint8_t* out_stage = slice_ring + C::NS * C::SLICE_STAGE;  // one 4 KB block per epilogue warp
+    uint8_t* slice_ring = smem + NF * FP32_STAGE_BYTES;
+    uint8_t* out_stage = slice_ring + NS * C::SLICE_STAGE;  // one block per epilogue warp
     uint64_t* bars = reinterpret_cast<uint64_t*>(out_stage + NUM_EPI_WARPS * STAGE_OUT_BYTES);
     uint64_t* fp32_full = bars;
-    uint64_t* fp32_empty = fp32_full + C::NF;
-    uint64_t* slice_full = fp32_empty + C::NF;   // leader: both CTAs' split warps
-    uint64_t* slice_empty = slice_full + C::NS;  // multicast commit
-    uint64_t* acc_full = slice_empty + C::NS;    // multicast commit
+    uint64_t* fp32_empty = fp32_full + NF;
+    uint64_t* slice_full = fp32_empty + NF;   // leader: both CTAs' split warps
+    uint64_t* slice_empty = slice_full + NS;  // multicast commit
+    uint64_t* acc_full = slice_empty + NS;    // multicast commit
     uint64_t* acc_empty = acc_full + 2;          // leader: both CTAs' epilogue warps
     uint64_t* drain = acc_empty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -300,17 +317,36 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
     const uint32_t rank = cluster_ctarank();
     const uint32_t cid = cluster_id_x(), ncl = num_clusters_x();
 
+    // The producer's TMA loads for the first FP32 stages need nothing but this
+    // CTA's own barriers, so they go out before the pair synchronises and
+    // allocates TMEM (the load latency overlaps the set-up).
+    auto issue_load = [&](int s, int tile, int ks) {
+        const int m0 = (tile / p.tiles_n) * TILE_M + HALF * rank;
+        const int n0 = (tile % p.tiles_n) * TILE_N + HALF * rank;
+        uint64_t* full = &fp32_full[s];
+        mbar_arrive_expect_tx(full, FP32_STAGE_BYTES);
+        uint8_t* dA = fp32_ring + s * FP32_STAGE_BYTES;
+        uint8_t* dB = dA + FP32_TILE_BYTES;
+        const int k0 = ks * BK;
+        if (!p.a_mn_major) tma_load_2d(dA, &p.tmA, full, k0, m0);
+        else for (int j = 0; j < 4; ++j) tma_load_2d(dA + j * 4096, &p.tmA, full, m0 + 32 * j, k0);
+        if (!p.b_mn_major) tma_load_2d(dB, &p.tmB, full, k0, n0);
+        else for (int j = 0; j < 4; ++j) tma_load_2d(dB + j * 4096, &p.tmB, full, n0 + 32 * j, k0);
+    };
+    int early = 0;  // stages already issued by thread 0 (warp 0 lane 0, the producer)
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::NF; ++s) { mbar_init(&fp32_full[s], 1); mbar_init(&fp32_empty[s], 1); }
-        for (int s = 0; s < C::NS; ++s) { mbar_init(&slice_full[s], 2); mbar_init(&slice_empty[s], 1); }
+        tma_prefetch_desc(&p.tmA);
+        tma_prefetch_desc(&p.tmB);
+        for (int s = 0; s < NF; ++s) { mbar_init(&fp32_full[s], 1); mbar_init(&fp32_empty[s], 1); }
+        for (int s = 0; s < NS; ++s) { mbar_init(&slice_full[s], 2); mbar_init(&slice_empty[s], 1); }
         for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 2); }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
-    }
-    if (warp == WARP_PRODUCER && lane == 0) {
-        tma_prefetch_desc(&p.tmA);
-        tma_prefetch_desc(&p.tmB);
+        for (int u = cid; early < NF && u < p.num_units; u += ncl) {
+            const Unit w = unit_of(p, u);
+            for (int ks = w.kb; early < NF && ks < w.ke; ++ks, ++early) issue_load(early, w.tile, ks);
+        }
     }
     if (warp == WARP_MMA) {
         tmem_alloc_pair(tmem_slot, TMEM_COLS);
@@ -326,32 +362,24 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         // ------------------------------------------------------ producer ----
         setmaxnreg_dec72();
         if (lane == 0) {
-            int s = 0;
+            int s = 0, n = 0;
             uint32_t ph = 0, issued_mask = 0, issued_parity = 0;
             bool ok = true;
             for (int u = cid; ok && u < p.num_units; u += ncl) {
                 const Unit w = unit_of(p, u);
-                const int m0 = (w.tile / p.tiles_n) * TILE_M + HALF * rank;
-                const int n0 = (w.tile % p.tiles_n) * TILE_N + HALF * rank;
-                for (int ks = w.kb; ks < w.ke; ++ks) {
-                    if (!mbar_wait(&fp32_empty[s], ph ^ 1u, abort_flag, budget, 1)) { ok = false; break; }
-                    uint64_t* full = &fp32_full[s];
-                    mbar_arrive_expect_tx(full, FP32_STAGE_BYTES);
-                    uint8_t* dA = fp32_ring + s * FP32_STAGE_BYTES;
-                    uint8_t* dB = dA + FP32_TILE_BYTES;
-                    const int k0 = ks * BK;
-                    if (!p.a_mn_major) tma_load_2d(dA, &p.tmA, full, k0, m0);
-                    else for (int j = 0; j < 4; ++j) tma_load_2d(dA + j * 4096, &p.tmA, full, m0 + 32 * j, k0);
-                    if (!p.b_mn_major) tma_load_2d(dB, &p.tmB, full, k0, n0);
-                    else for (int j = 0; j < 4; ++j) tma_load_2d(dB + j * 4096, &p.tmB, full, n0 + 32 * j, k0);
+                for (int ks = w.kb; ks < w.ke; ++ks, ++n) {
+                    if (n >= early) {  // the first `early` loads went out before the pair sync
+                        if (!mbar_wait(&fp32_empty[s], ph ^ 1u, abort_flag, budget, 1)) { ok = false; break; }
+                        issue_load(s, w.tile, ks);
+                    }
                     issued_mask |= 1u << s;
                     issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
-                    if (++s == C::NF) { s = 0; ph ^= 1u; }
+                    if (++s == NF) { s = 0; ph ^= 1u; }
                 }
             }
             if (!ok) {
                 // give every load already in flight time to land before the CTA exits
-                for (int t = 0; t < C::NF; ++t)
+                for (int t = 0; t < NF; ++t)
                     if (issued_mask & (1u << t)) {
                         volatile int never = 0;
                         mbar_wait(&fp32_full[t], (issued_parity >> t) & 1u, &never, 50000000ull, 1);
@@ -379,7 +407,7 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                     issued = true;
                     mma_commit_pair_multicast(&slice_empty[s], 0x3);
                     mma_commit_pair_multicast(&acc_full[b], 0x3);
-                    if (++s == C::NS) { s = 0; ph ^= 1u; }
+                    if (++s == NS) { s = 0; ph ^= 1u; }
                     if (++b == 2) { b = 0; bph ^= 1u; }
                 }
             }
@@ -417,8 +445,8 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                     if (rank == 0) mbar_arrive(&slice_full[ss]);
                     else mbar_arrive_cluster(&slice_full[ss], 0);
                 }
-                if (++fs == C::NF) { fs = 0; fph ^= 1u; }
-                if (++ss == C::NS) { ss = 0; sph ^= 1u; }
+                if (++fs == NF) { fs = 0; fph ^= 1u; }
+                if (++ss == NS) { ss = 0; sph ^= 1u; }
             }
         }
     } else {
@@ -507,23 +535,29 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                     }
                 }
             }
-            // 4 blocks of 32 x 32: each lane stages its row's 32 sums in shared
-            // memory (128-byte rows, 128-byte swizzle); the warp then reads them
-            // back as 4 whole row segments per pass, applies
-            // C = alpha * acc + beta * C_old + bias and stores 128 contiguous
-            // bytes per row (coalesced), clipping rows and columns outside C.
+            // 128 / OUT_COLS blocks of 32 rows x OUT_COLS columns: each lane stages
+            // its row's sums in shared memory (rows of OUT_COLS * 4 bytes, 16-byte
+            // chunks XOR-swizzled by row); the warp then reads them back as whole
+            // row segments, applies C = alpha * acc + beta * C_old + bias and
+            // stores the rows contiguously (coalesced), clipping rows and columns
+            // outside C.
+            constexpr int CPR = OUT_COLS / 4;   // 16-byte chunks per staged row
+            constexpr int RPP = 32 / CPR;       // rows per read-back pass
             uint8_t* stage = out_stage + e * STAGE_OUT_BYTES;
             const float alpha = p.alpha, beta = p.beta;
-            const uint32_t q = lane & 7u;
+            const uint32_t q = lane % CPR;
+            auto chunk_off = [](uint32_t r, uint32_t j) {
+                return OUT_COLS == 32 ? off_f32_chunk(r, j) : off_bf16_chunk(r, j);
+            };
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 128 / OUT_COLS; ++c) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    *reinterpret_cast<float4*>(stage + off_f32_chunk(lane, j)) =
-                        make_float4(acc[32 * c + 4 * j], acc[32 * c + 4 * j + 1], acc[32 * c + 4 * j + 2],
-                                    acc[32 * c + 4 * j + 3]);
+                for (int j = 0; j < CPR; ++j)
+                    *reinterpret_cast<float4*>(stage + chunk_off(lane, j)) =
+                        make_float4(acc[OUT_COLS * c + 4 * j], acc[OUT_COLS * c + 4 * j + 1],
+                                    acc[OUT_COLS * c + 4 * j + 2], acc[OUT_COLS * c + 4 * j + 3]);
                 __syncwarp();
-                const int gcol = col0 + 32 * c + static_cast<int>(4 * q);  // this lane's 4 columns
+                const int gcol = col0 + OUT_COLS * c + static_cast<int>(4 * q);  // this lane's 4 columns
                 const bool full4 = gcol + 3 < p.N;
                 float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);
                 if (p.bias) {
@@ -536,9 +570,9 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                     }
                 }
 #pragma unroll
-                for (int pass = 0; pass < 8; ++pass) {
-                    const uint32_t rr = pass * 4u + (lane >> 3);
-                    const float4 v = *reinterpret_cast<const float4*>(stage + off_f32_chunk(rr, q));
+                for (int pass = 0; pass < 32 / RPP; ++pass) {
+                    const uint32_t rr = pass * RPP + lane / CPR;
+                    const float4 v = *reinterpret_cast<const float4*>(stage + chunk_off(rr, q));
                     const int grow = row0 + static_cast<int>(rr);
                     if (grow >= p.M) continue;
                     float* dst = p.c + static_cast<long long>(grow) * p.ldc + gcol;
