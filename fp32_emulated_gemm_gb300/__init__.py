@@ -19,9 +19,9 @@ import threading
 
 __all__ = [
     "EMU_MODE_BF16X9", "EMU_MODE_TF32X3", "EMU_OP_N", "EMU_OP_T", "EmuError",
-    "emu_sgemm", "emu_linear_fwd", "emu_linear_bwd_input", "emu_status_string",
+    "emu_sgemm", "emu_linear_fwd", "emu_linear_bwd_input", "emu_linear_bwd_weight", "emu_status_string",
     "emu_stream_check", "emu_split_dump", "emu_version",
-    "sgemm", "linear_fwd", "linear_bwd_input", "EmuLinearFunction", "EmuLinear",
+    "sgemm", "linear_fwd", "linear_bwd_input", "linear_bwd_weight", "EmuLinearFunction", "EmuLinear",
     "library_path", "load",
 ]
 
@@ -67,12 +67,14 @@ def load():
         L.emu_sgemm.argtypes = [i32, i32, i32, i64, i64, i64, f32, P, i64, P, i64, f32, P, i64, P]
         L.emu_linear_fwd.argtypes = [i32, i64, i64, i64, P, P, P, P, P]
         L.emu_linear_bwd_input.argtypes = [i32, i64, i64, i64, P, P, P, P]
+        L.emu_linear_bwd_weight.argtypes = [i32, i64, i64, i64, P, P, f32, P, P]
         L.emu_status_string.argtypes = [i32]
         L.emu_status_string.restype = ctypes.c_char_p
         L.emu_stream_check.argtypes = [P]
         L.emu_split_dump.argtypes = [i32, i64, i64, P, i64, i32, P, P]
         L.emu_version.argtypes = []
-        for name in ("emu_sgemm", "emu_linear_fwd", "emu_linear_bwd_input", "emu_stream_check",
+        for name in ("emu_sgemm", "emu_linear_fwd", "emu_linear_bwd_input", "emu_linear_bwd_weight",
+                     "emu_stream_check",
                      "emu_split_dump", "emu_version"):
             getattr(L, name).restype = i32
         _lib = L
@@ -110,6 +112,11 @@ def emu_linear_fwd(mode, M, N, K, X, W, bias, Y, stream=None):
 def emu_linear_bwd_input(mode, M, N, K, dY, W, dX, stream=None):
     _check(load().emu_linear_bwd_input(int(mode), int(M), int(N), int(K), _ptr(dY), _ptr(W), _ptr(dX),
                                        ctypes.c_void_p(_stream(stream))), "emu_linear_bwd_input")
+
+
+def emu_linear_bwd_weight(mode, M, N, K, dY, X, beta, dW, stream=None):
+    _check(load().emu_linear_bwd_weight(int(mode), int(M), int(N), int(K), _ptr(dY), _ptr(X), float(beta),
+                                        _ptr(dW), ctypes.c_void_p(_stream(stream))), "emu_linear_bwd_weight")
 
 
 def emu_status_string(status: int) -> str:
@@ -182,18 +189,29 @@ def linear_bwd_input(dY, W, *, mode="bf16x9", out=None):
     return dX
 
 
+def linear_bwd_weight(dY, X, *, mode="bf16x9", out=None, beta=0.0):
+    """dW = dY^T X (+ beta * out) (dY [M,N], X [M,K], contiguous)."""
+    import torch
+    M, N = dY.shape
+    K = X.shape[1]
+    dW = out if out is not None else torch.empty((N, K), device=dY.device, dtype=torch.float32)
+    emu_linear_bwd_weight(_mode(mode), M, N, K, dY.contiguous(), X.contiguous(), beta, dW)
+    return dW
+
+
 def _autograd():
     import torch
 
     class EmuLinearFunction(torch.autograd.Function):
         """nn.Linear with the forward and the input gradient emulated; the
         weight gradient uses plain FP32 (TF32 off), as in the blog's
-        TF32Linear ("TF32x3 on Ampere GPUs")."""
+        TF32Linear ("TF32x3 on Ampere GPUs"), unless weight_grad="emulated"."""
 
         @staticmethod
-        def forward(ctx, X, W, bias, mode):
+        def forward(ctx, X, W, bias, mode, weight_grad="fp32"):
             ctx.save_for_backward(X, W)
             ctx.mode = mode
+            ctx.weight_grad = weight_grad
             ctx.has_bias = bias is not None
             return linear_fwd(X, W, bias, mode=mode)
 
@@ -203,7 +221,9 @@ def _autograd():
             dY = dY.contiguous()
             dX = linear_bwd_input(dY, W, mode=ctx.mode) if ctx.needs_input_grad[0] else None
             dW = db = None
-            if ctx.needs_input_grad[1]:
+            if ctx.needs_input_grad[1] and ctx.weight_grad == "emulated":
+                dW = linear_bwd_weight(dY, X, mode=ctx.mode)
+            elif ctx.needs_input_grad[1]:
                 prev = torch.backends.cuda.matmul.allow_tf32
                 torch.backends.cuda.matmul.allow_tf32 = False
                 try:
@@ -212,18 +232,20 @@ def _autograd():
                     torch.backends.cuda.matmul.allow_tf32 = prev
             if ctx.has_bias and ctx.needs_input_grad[2]:
                 db = dY.sum(0)
-            return dX, dW, db, None
+            return dX, dW, db, None, None
 
     class EmuLinear(torch.nn.Linear):
         """Drop-in nn.Linear whose matmuls run on the emulated path."""
 
-        def __init__(self, in_features, out_features, bias=True, mode="bf16x9", **kw):
+        def __init__(self, in_features, out_features, bias=True, mode="bf16x9", weight_grad="fp32", **kw):
             super().__init__(in_features, out_features, bias=bias, **kw)
             self.mode = mode
+            self.weight_grad = weight_grad
 
         def forward(self, x):
             shp = x.shape
-            y = EmuLinearFunction.apply(x.reshape(-1, shp[-1]), self.weight, self.bias, self.mode)
+            y = EmuLinearFunction.apply(x.reshape(-1, shp[-1]), self.weight, self.bias, self.mode,
+                                        self.weight_grad)
             return y.reshape(*shp[:-1], self.out_features)
 
     return EmuLinearFunction, EmuLinear

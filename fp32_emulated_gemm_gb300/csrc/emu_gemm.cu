@@ -24,6 +24,16 @@ namespace {
 
 constexpr unsigned long long kDefaultWaitBudgetNs = 2000000000ull;  // 2 s per wait
 
+// EMU_LOG=1 prints each launch's plan (tiles, split, grid) to stderr.
+bool log_enabled() {
+    static const bool on = [] {
+        const char* s = std::getenv("EMU_LOG");
+        return s && s[0] && s[0] != '0';
+    }();
+    return on;
+}
+
+
 struct DeviceInfo {
     bool ready = false;
     int cc_major = 0, cc_minor = 0, sm_count = 0;
@@ -52,8 +62,19 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 emu_status_t device_info(DeviceInfo** out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    const cudaError_t ge = cudaGetDevice(&dev);
+    if (ge != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();
+        if (log_enabled()) std::fprintf(stderr, "[emu] cudaGetDevice: %s (device %d)\n", cudaGetErrorName(ge), dev);
+        return EMU_STATUS_LAUNCH_FAILED;
+    }
+    // Bind the device's primary context to this host thread: a thread that has
+    // not made a runtime call yet (e.g. an autograd worker) has none current,
+    // and encoding a TMA tensor map needs one.
+    const cudaError_t se = cudaSetDevice(dev);
+    if (se != cudaSuccess) {
+        cudaGetLastError();
+        if (log_enabled()) std::fprintf(stderr, "[emu] cudaSetDevice: %s\n", cudaGetErrorName(se));
         return EMU_STATUS_LAUNCH_FAILED;
     }
     std::lock_guard<std::mutex> lock(g_mutex);
@@ -124,9 +145,14 @@ bool encode_f32_2d(CUtensorMap* map, const float* base, uint64_t inner, uint64_t
     const cuuint64_t strides[1] = {ld * sizeof(float)};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides,
+                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS && log_enabled())
+        std::fprintf(stderr, "[emu] tensor map encode failed (%d): base %p dims %llu x %llu ld %llu box %u x %u\n",
+                     (int)r, (const void*)base, (unsigned long long)inner, (unsigned long long)outer,
+                     (unsigned long long)ld, box_inner, box_outer);
+    return r == CUDA_SUCCESS;
 }
 
 // op(X) tile map: K-major operands (rows of K) load {32 k, 128 rows};
@@ -175,7 +201,7 @@ emu_status_t workspace_for(int dev, cudaStream_t stream, size_t floats, size_t c
             if (c.device < 0) { w = &c; w->device = dev; w->stream = stream; break; }
     if (!w) return EMU_STATUS_ALLOC_FAILED;
     if (w->partial_floats < floats) {
-        if (w->partials) cudaFreeAsync(w->partials, stream);
+        if (w->partials && cudaFreeAsync(w->partials, stream) != cudaSuccess) cudaGetLastError();
         w->partials = nullptr;
         w->partial_floats = 0;
         if (cudaMallocAsync(reinterpret_cast<void**>(&w->partials), floats * sizeof(float), stream) != cudaSuccess) {
@@ -185,7 +211,7 @@ emu_status_t workspace_for(int dev, cudaStream_t stream, size_t floats, size_t c
         w->partial_floats = floats;
     }
     if (w->num_counters < counters) {
-        if (w->counters) cudaFreeAsync(w->counters, stream);
+        if (w->counters && cudaFreeAsync(w->counters, stream) != cudaSuccess) cudaGetLastError();
         w->counters = nullptr;
         w->num_counters = 0;
         if (cudaMallocAsync(reinterpret_cast<void**>(&w->counters), counters * sizeof(int), stream) != cudaSuccess ||
@@ -212,7 +238,7 @@ int choose_split_k(int tiles, int k_stages, int pairs) {
     }
     int best = 1;
     double best_cost = -1.0;
-    for (int S = 1; S <= 8 && S <= k_stages; ++S) {
+    for (int S = 1; S <= 64 && S <= k_stages; ++S) {
         if (S > 1 && k_stages / S < 2) break;
         const long long units = (long long)tiles * S;
         const long long waves = (units + pairs - 1) / pairs;
@@ -222,15 +248,6 @@ int choose_split_k(int tiles, int k_stages, int pairs) {
         if (best_cost < 0 || cost < best_cost - 1e-9) { best_cost = cost; best = S; }
     }
     return best;
-}
-
-// EMU_LOG=1 prints each launch's plan (tiles, split, grid) to stderr.
-bool log_enabled() {
-    static const bool on = [] {
-        const char* s = std::getenv("EMU_LOG");
-        return s && s[0] && s[0] != '0';
-    }();
-    return on;
 }
 
 unsigned long long wait_budget_ns() {
@@ -246,19 +263,30 @@ unsigned long long wait_budget_ns() {
 // wider output staging (see PipeCfg).
 constexpr int kLongKMinStages = 16;
 
+// The launch's own status (cudaLaunchKernelEx), so that an error left by an
+// unrelated earlier runtime call on this host thread is not reported as ours.
 cudaError_t launch_gemm(emu_mode_t mode, const Params& p, int clusters, cudaStream_t stream) {
-    const dim3 grid(2 * clusters, 1, 1);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.stream = stream;
     const int per_unit = (p.k_stages + p.split_k - 1) / p.split_k;
-    if (mode == EMU_MODE_TF32X3)
-        emu_gemm_kernel<MODE_TF32X3, PIPE_SHORT_K>
-            <<<grid, NUM_THREADS, smem_bytes<MODE_TF32X3, PIPE_SHORT_K>(), stream>>>(p);
-    else if (per_unit >= kLongKMinStages)
-        emu_gemm_kernel<MODE_BF16X9, PIPE_LONG_K>
-            <<<grid, NUM_THREADS, smem_bytes<MODE_BF16X9, PIPE_LONG_K>(), stream>>>(p);
-    else
-        emu_gemm_kernel<MODE_BF16X9, PIPE_SHORT_K>
-            <<<grid, NUM_THREADS, smem_bytes<MODE_BF16X9, PIPE_SHORT_K>(), stream>>>(p);
-    return cudaGetLastError();
+    cudaError_t e;
+    if (mode == EMU_MODE_TF32X3) {
+        cfg.dynamicSmemBytes = smem_bytes<MODE_TF32X3, PIPE_SHORT_K>();
+        e = cudaLaunchKernelEx(&cfg, emu_gemm_kernel<MODE_TF32X3, PIPE_SHORT_K>, p);
+    } else if (per_unit >= kLongKMinStages) {
+        cfg.dynamicSmemBytes = smem_bytes<MODE_BF16X9, PIPE_LONG_K>();
+        e = cudaLaunchKernelEx(&cfg, emu_gemm_kernel<MODE_BF16X9, PIPE_LONG_K>, p);
+    } else {
+        cfg.dynamicSmemBytes = smem_bytes<MODE_BF16X9, PIPE_SHORT_K>();
+        e = cudaLaunchKernelEx(&cfg, emu_gemm_kernel<MODE_BF16X9, PIPE_SHORT_K>, p);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        if (log_enabled()) std::fprintf(stderr, "[emu] launch failed: %s\n", cudaGetErrorName(e));
+    }
+    return e;
 }
 
 // Core: C = alpha * op(A) op(B) + beta * C_old + bias, with C_old == C.
@@ -290,6 +318,7 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
         const int threads = 256;
         const int64_t blocks64 = (total + threads - 1) / threads;
         const int blocks = (int)(blocks64 < dev->sm_count * 8 ? blocks64 : dev->sm_count * 8);
+        cudaGetLastError();  // only this launch's status below
         scale_kernel<<<blocks, threads, 0, stream>>>(M, N, beta, C, ldc, bias);
         return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
     }
@@ -369,6 +398,22 @@ __global__ void __launch_bounds__(256, 1) split_dump_kernel(const __grid_constan
     }
 }
 
+// Self-test of the bounded waits: one warp waits on a barrier that nothing
+// arrives on, with the caller's budget, through the same routine the GEMM
+// kernel's split and epilogue warps use.  The wait gives up, records the
+// timeout in the device error word and the kernel returns normally.
+__global__ void wait_timeout_selftest_kernel(unsigned long long budget_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncwarp();
+    mbar_wait_warp(&bar, 0, &abort_flag, budget_ns, 7);
+}
+
 }  // namespace
 }  // namespace emu
 
@@ -398,6 +443,14 @@ emu_status_t emu_linear_bwd_input(emu_mode_t mode, int64_t M, int64_t N, int64_t
     // dX[M,K] = dY[M,N] W[N,K]: GEMM with output width K and contraction N;
     // op(B) = W is MN-major (rows are the contraction index)
     return run_gemm(mode, false, true, M, K, N, 1.0f, dY, N, W, K, 0.0f, dX, K, nullptr,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+emu_status_t emu_linear_bwd_weight(emu_mode_t mode, int64_t M, int64_t N, int64_t K, const float* dY,
+                                   const float* X, float beta, float* dW, emu_stream_t stream) {
+    // dW[N,K] = dY^T X: output rows N, output columns K, contraction M; both
+    // operands are MN-major (their rows are the contraction index)
+    return run_gemm(mode, true, true, N, K, M, 1.0f, dY, N, X, K, beta, dW, K, nullptr,
                     reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -438,12 +491,24 @@ emu_status_t emu_split_dump(emu_mode_t mode, int64_t R, int64_t Kc, const float*
     if (mode == EMU_MODE_BF16X9) {
         const uint32_t bytes = 1024 + FP32_TILE_BYTES + 3 * Cfg<MODE_BF16X9>::COMP_TILE + 64;
         cudaFuncSetAttribute(split_dump_kernel<MODE_BF16X9>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        cudaGetLastError();
         split_dump_kernel<MODE_BF16X9><<<1, 256, bytes, s>>>(tm, R32, K32, mn_major, out);
     } else {
         const uint32_t bytes = 1024 + FP32_TILE_BYTES + 2 * Cfg<MODE_TF32X3>::COMP_TILE + 64;
         cudaFuncSetAttribute(split_dump_kernel<MODE_TF32X3>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        cudaGetLastError();
         split_dump_kernel<MODE_TF32X3><<<1, 256, bytes, s>>>(tm, R32, K32, mn_major, out);
     }
+    return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
+}
+
+emu_status_t emu_selftest_wait_timeout(uint64_t budget_ns, emu_stream_t stream) {
+    if (budget_ns == 0 || budget_ns > 10000000000ull) return EMU_STATUS_INVALID_VALUE;
+    DeviceInfo* dev = nullptr;
+    emu_status_t st = device_info(&dev);
+    if (st != EMU_STATUS_SUCCESS) return st;
+    cudaGetLastError();
+    wait_timeout_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(budget_ns);
     return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
 }
 
@@ -519,6 +584,7 @@ emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, 
         const int threads = 256;
         const int64_t blocks64 = (total + threads - 1) / threads;
         const int blocks = (int)(blocks64 < dev->sm_count * 8 ? blocks64 : dev->sm_count * 8);
+        cudaGetLastError();
         scale_kernel<<<blocks, threads, 0, stream>>>(M, N, beta, C, ldc, nullptr);
         return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
     }

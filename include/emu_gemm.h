@@ -118,6 +118,18 @@ emu_status_t emu_linear_bwd_input(emu_mode_t mode, int64_t M, int64_t N, int64_t
                                   const float *dY, const float *W, float *dX,
                                   emu_stream_t stream);
 
+/*
+ * emu_linear_bwd_weight -- dW[N,K] = dY[M,N]^T * X[M,K] + beta * dW.
+ *   The weight-gradient pass of the same layer, emulated: the contraction
+ *   runs over the M tokens.  The blog computes this pass with standard FP32
+ *   ("TF32x3 on Ampere GPUs": not needed for fixed-weight inference); it is
+ *   offered here for training with the same arithmetic.  beta = 1
+ *   accumulates into an existing gradient; beta = 0 never reads dW.
+ */
+emu_status_t emu_linear_bwd_weight(emu_mode_t mode, int64_t M, int64_t N, int64_t K,
+                                   const float *dY, const float *X, float beta, float *dW,
+                                   emu_stream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *emu_status_string(emu_status_t s);
 
@@ -182,6 +194,16 @@ emu_status_t emu_sgemm_noalloc(emu_mode_t mode, emu_op_t transA, emu_op_t transB
                                float alpha, const float *A, int64_t lda,
                                const float *B, int64_t ldb,
                                float beta, float *C, int64_t ldc, emu_stream_t stream);
+
+/*
+ * emu_selftest_wait_timeout -- diagnostic for the device-side failure path:
+ * launches one warp that waits, through the same bounded-wait routine as the
+ * GEMM kernels, on a barrier that nothing ever completes.  After budget_ns
+ * nanoseconds (0 < budget_ns <= 10 s) the wait gives up and the kernel
+ * returns; the next emu_stream_check() on this stream reports
+ * EMU_STATUS_DEVICE_TIMEOUT and clears the flag.  No fault, trap or hang.
+ */
+emu_status_t emu_selftest_wait_timeout(uint64_t budget_ns, emu_stream_t stream);
 
 /* Library version as an integer (major * 10000 + minor * 100 + patch). */
 int emu_version(void);
