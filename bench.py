@@ -37,7 +37,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--mode", default="bf16x9", choices=["bf16x9", "tf32x3"])
+    ap.add_argument("--mode", default="bf16x9", choices=["bf16x9", "tf32x3", "tf32x1", "bf16x6"])
     ap.add_argument("--workload", default="pet_small", choices=["pet_small", "pet_large", "wide_l1", "wide_l2"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
@@ -278,7 +278,9 @@ def main():
     value = world * flops / (step_ms * 1e-3) / 1e12
 
     peaks, peak_kind = load_peaks()
-    peak = peaks["bf16_tflops"] / (9.0 if args.mode == "bf16x9" else 6.0)
+    # tensor work per effective FLOP, in BF16-rate units (TF32 runs at half rate)
+    tensor_units = {"bf16x9": 9.0, "bf16x6": 6.0, "tf32x3": 6.0, "tf32x1": 2.0}[args.mode]
+    peak = peaks["bf16_tflops"] / tensor_units
     # dominant kernel: the emulated-GEMM kernel (both launches of a step);
     # algorithmic work per launch = 2 M N K effective FLOPs
     achieved = (flops / 2) / ((step_ms / 2) * 1e-3) / 1e12
@@ -299,11 +301,11 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16x9" if args.mode == "bf16x9" else "tf32x3", "data": "synthetic",
+        "dtype": args.mode, "data": "synthetic",
         "config": workload_config(args, s),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_kind} bf16 dense burst / {9 if args.mode == 'bf16x9' else 6}",
+                     "peak_source": f"{peak_kind} bf16 dense burst / {tensor_units:g}",
                      "kernel": f"emu_gemm_kernel<{args.mode}>", "fwd_ms": sum(t_fwd) / K,
                      "bwd_ms": sum(t_bwd) / K},
         "gpu_launches": 2 * K,

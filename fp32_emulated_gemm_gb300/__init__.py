@@ -18,7 +18,8 @@ import os
 import threading
 
 __all__ = [
-    "EMU_MODE_BF16X9", "EMU_MODE_TF32X3", "EMU_OP_N", "EMU_OP_T", "EmuError",
+    "EMU_MODE_BF16X9", "EMU_MODE_TF32X3", "EMU_MODE_TF32X1", "EMU_MODE_BF16X6", "EMU_OP_N", "EMU_OP_T",
+    "EmuError",
     "emu_sgemm", "emu_linear_fwd", "emu_linear_bwd_input", "emu_linear_bwd_weight", "emu_status_string",
     "emu_stream_check", "emu_split_dump", "emu_version",
     "sgemm", "linear_fwd", "linear_bwd_input", "linear_bwd_weight", "EmuLinearFunction", "EmuLinear",
@@ -27,9 +28,12 @@ __all__ = [
 
 EMU_MODE_BF16X9 = 0
 EMU_MODE_TF32X3 = 1
+EMU_MODE_TF32X1 = 2
+EMU_MODE_BF16X6 = 3
 EMU_OP_N = 0
 EMU_OP_T = 1
-MODES = {"bf16x9": EMU_MODE_BF16X9, "tf32x3": EMU_MODE_TF32X3}
+MODES = {"bf16x9": EMU_MODE_BF16X9, "tf32x3": EMU_MODE_TF32X3, "tf32x1": EMU_MODE_TF32X1,
+         "bf16x6": EMU_MODE_BF16X6}
 
 STATUS_NAMES = {
     0: "EMU_STATUS_SUCCESS", 1: "EMU_STATUS_INVALID_VALUE", 2: "EMU_STATUS_NOT_SUPPORTED",

@@ -60,6 +60,27 @@ std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+template <int MODE, int PIPE>
+cudaError_t set_smem_attr() {
+    return cudaFuncSetAttribute(emu_gemm_kernel<MODE, PIPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem_bytes<MODE, PIPE>());
+}
+
+bool valid_mode(emu_mode_t mode) {
+    return mode == EMU_MODE_BF16X9 || mode == EMU_MODE_TF32X3 || mode == EMU_MODE_TF32X1 ||
+           mode == EMU_MODE_BF16X6;
+}
+
+const char* mode_name(emu_mode_t mode) {
+    switch (mode) {
+        case EMU_MODE_BF16X9: return "bf16x9";
+        case EMU_MODE_TF32X3: return "tf32x3";
+        case EMU_MODE_TF32X1: return "tf32x1";
+        case EMU_MODE_BF16X6: return "bf16x6";
+    }
+    return "?";
+}
+
 emu_status_t device_info(DeviceInfo** out) {
     int dev = 0;
     const cudaError_t ge = cudaGetDevice(&dev);
@@ -100,15 +121,12 @@ emu_status_t device_info(DeviceInfo** out) {
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     if (!d.attrs_set) {
-        if (cudaFuncSetAttribute(emu_gemm_kernel<MODE_BF16X9, PIPE_SHORT_K>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_bytes<MODE_BF16X9, PIPE_SHORT_K>()) != cudaSuccess ||
-            cudaFuncSetAttribute(emu_gemm_kernel<MODE_BF16X9, PIPE_LONG_K>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_bytes<MODE_BF16X9, PIPE_LONG_K>()) != cudaSuccess ||
-            cudaFuncSetAttribute(emu_gemm_kernel<MODE_TF32X3, PIPE_SHORT_K>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_bytes<MODE_TF32X3, PIPE_SHORT_K>()) != cudaSuccess) {
+        if (set_smem_attr<MODE_BF16X9, PIPE_SHORT_K>() != cudaSuccess ||
+            set_smem_attr<MODE_BF16X9, PIPE_LONG_K>() != cudaSuccess ||
+            set_smem_attr<MODE_BF16X6, PIPE_SHORT_K>() != cudaSuccess ||
+            set_smem_attr<MODE_BF16X6, PIPE_LONG_K>() != cudaSuccess ||
+            set_smem_attr<MODE_TF32X3, PIPE_SHORT_K>() != cudaSuccess ||
+            set_smem_attr<MODE_TF32X1, PIPE_SHORT_K>() != cudaSuccess) {
             cudaGetLastError();
             return EMU_STATUS_LAUNCH_FAILED;
         }
@@ -263,6 +281,12 @@ unsigned long long wait_budget_ns() {
 // wider output staging (see PipeCfg).
 constexpr int kLongKMinStages = 16;
 
+template <int MODE, int PIPE>
+cudaError_t launch_one(cudaLaunchConfig_t cfg, const Params& p) {
+    cfg.dynamicSmemBytes = smem_bytes<MODE, PIPE>();
+    return cudaLaunchKernelEx(&cfg, emu_gemm_kernel<MODE, PIPE>, p);
+}
+
 // The launch's own status (cudaLaunchKernelEx), so that an error left by an
 // unrelated earlier runtime call on this host thread is not reported as ours.
 cudaError_t launch_gemm(emu_mode_t mode, const Params& p, int clusters, cudaStream_t stream) {
@@ -271,16 +295,16 @@ cudaError_t launch_gemm(emu_mode_t mode, const Params& p, int clusters, cudaStre
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.stream = stream;
     const int per_unit = (p.k_stages + p.split_k - 1) / p.split_k;
+    const bool long_k = per_unit >= kLongKMinStages;
     cudaError_t e;
-    if (mode == EMU_MODE_TF32X3) {
-        cfg.dynamicSmemBytes = smem_bytes<MODE_TF32X3, PIPE_SHORT_K>();
-        e = cudaLaunchKernelEx(&cfg, emu_gemm_kernel<MODE_TF32X3, PIPE_SHORT_K>, p);
-    } else if (per_unit >= kLongKMinStages) {
-        cfg.dynamicSmemBytes = smem_bytes<MODE_BF16X9, PIPE_LONG_K>();
-        e = cudaLaunchKernelEx(&cfg, emu_gemm_kernel<MODE_BF16X9, PIPE_LONG_K>, p);
-    } else {
-        cfg.dynamicSmemBytes = smem_bytes<MODE_BF16X9, PIPE_SHORT_K>();
-        e = cudaLaunchKernelEx(&cfg, emu_gemm_kernel<MODE_BF16X9, PIPE_SHORT_K>, p);
+    switch (mode) {
+        case EMU_MODE_TF32X3: e = launch_one<MODE_TF32X3, PIPE_SHORT_K>(cfg, p); break;
+        case EMU_MODE_TF32X1: e = launch_one<MODE_TF32X1, PIPE_SHORT_K>(cfg, p); break;
+        case EMU_MODE_BF16X6:
+            e = long_k ? launch_one<MODE_BF16X6, PIPE_LONG_K>(cfg, p) : launch_one<MODE_BF16X6, PIPE_SHORT_K>(cfg, p);
+            break;
+        default:
+            e = long_k ? launch_one<MODE_BF16X9, PIPE_LONG_K>(cfg, p) : launch_one<MODE_BF16X9, PIPE_SHORT_K>(cfg, p);
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -293,7 +317,7 @@ cudaError_t launch_gemm(emu_mode_t mode, const Params& p, int clusters, cudaStre
 emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t N, int64_t K, float alpha,
                       const float* A, int64_t lda, const float* B, int64_t ldb, float beta, float* C,
                       int64_t ldc, const float* bias, cudaStream_t stream) {
-    if (mode != EMU_MODE_BF16X9 && mode != EMU_MODE_TF32X3) return EMU_STATUS_INVALID_VALUE;
+    if (!valid_mode(mode)) return EMU_STATUS_INVALID_VALUE;
     if (M < 0 || N < 0 || K < 0) return EMU_STATUS_INVALID_VALUE;
     if (M > INT32_MAX - 256 || N > INT32_MAX - 256 || K > INT32_MAX - 256) return EMU_STATUS_NOT_SUPPORTED;
     if (M == 0 || N == 0) return EMU_STATUS_SUCCESS;
@@ -332,7 +356,7 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
     p.tiles_n = (int)((N + TILE_N - 1) / TILE_N);
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.k_stages = (int)((K + BK - 1) / BK);
-    const int pairs = dev->max_clusters[mode == EMU_MODE_BF16X9 ? 0 : 1];
+    const int pairs = dev->max_clusters[mode == EMU_MODE_TF32X3 ? 1 : 0];
     p.split_k = choose_split_k(p.num_tiles, p.k_stages, pairs);
     p.num_units = p.num_tiles * p.split_k;
     p.alpha = alpha; p.beta = beta;
@@ -353,7 +377,7 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
     if (log_enabled())
         std::fprintf(stderr, "[emu] %s M=%lld N=%lld K=%lld a_mn=%d b_mn=%d tiles=%dx%d k_stages=%d split_k=%d "
                              "units=%d pairs=%d (max %d) long_k_pipe=%u\n",
-                     mode == EMU_MODE_BF16X9 ? "bf16x9" : "tf32x3", (long long)M, (long long)N, (long long)K,
+                     mode_name(mode), (long long)M, (long long)N, (long long)K,
                      (int)a_mn, (int)b_mn, p.tiles_m, p.tiles_n, p.k_stages, p.split_k, p.num_units, clusters,
                      pairs, (p.k_stages + p.split_k - 1) / p.split_k >= kLongKMinStages ? 1u : 0u);
     return launch_gemm(mode, p, clusters, stream) == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
@@ -559,7 +583,7 @@ emu_status_t noalloc_scratch(void** out) {
 emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t N, int64_t K,
                               float alpha, const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
                               float* C, int64_t ldc, cudaStream_t stream) {
-    if (mode != EMU_MODE_BF16X9 && mode != EMU_MODE_TF32X3) return EMU_STATUS_INVALID_VALUE;
+    if (!valid_mode(mode)) return EMU_STATUS_INVALID_VALUE;
     if (M < 0 || N < 0 || K < 0) return EMU_STATUS_INVALID_VALUE;
     if (M > INT32_MAX - 256 || N > INT32_MAX - 256 || K > INT32_MAX - 256) return EMU_STATUS_NOT_SUPPORTED;
     if (M == 0 || N == 0) return EMU_STATUS_SUCCESS;
@@ -598,7 +622,7 @@ emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, 
     p.tiles_n = (int)((N + TILE_N - 1) / TILE_N);
     p.num_tiles = p.tiles_m * p.tiles_n;
     p.k_stages = (int)((K + BK - 1) / BK);
-    const int pairs = dev->max_clusters[mode == EMU_MODE_BF16X9 ? 0 : 1];
+    const int pairs = dev->max_clusters[mode == EMU_MODE_TF32X3 ? 1 : 0];
     p.split_k = choose_split_k(p.num_tiles, p.k_stages, pairs);
     p.num_units = p.num_tiles * p.split_k;
     p.alpha = alpha; p.beta = beta;

@@ -46,7 +46,9 @@
 
 namespace emu {
 
-enum Mode : int { MODE_BF16X9 = 0, MODE_TF32X3 = 1 };
+// BF16x9 and TF32x3 are the method; BF16x6 (bands 0-2) and one-pass TF32
+// (hi*hi) are the faster, less accurate comparators.
+enum Mode : int { MODE_BF16X9 = 0, MODE_TF32X3 = 1, MODE_TF32X1 = 2, MODE_BF16X6 = 3 };
 
 constexpr int TILE_M = 256;       // rows of a pair tile (128 per CTA)
 constexpr int TILE_N = 256;       // columns of a pair tile (TMEM columns per accumulator)
@@ -68,20 +70,49 @@ constexpr uint32_t SPLIT_BARRIER = 2;       // named barrier of the split thread
 constexpr uint32_t FP32_TILE_BYTES = HALF * BK * 4;           // 16 KB
 constexpr uint32_t FP32_STAGE_BYTES = 2 * FP32_TILE_BYTES;    // 32 KB
 
+// Per mode: components per operand, their tile geometry, the MMA kind and
+// the (i, j) component products of a stage, smallest first (for BF16: band
+// i + j descending; for TF32: 0 = hi, 1 = lo).
 template <int MODE> struct Cfg;
-template <> struct Cfg<MODE_BF16X9> {
+struct CfgBF16 {
+    static constexpr bool TF32 = false;
     static constexpr int NCOMP = 3;                  // components per operand
     static constexpr uint32_t ROW_BYTES = BK * 2;    // 64: one BF16 row of a stage
     static constexpr uint32_t COMP_TILE = HALF * ROW_BYTES;         // 8 KB
     static constexpr uint32_t SLICE_STAGE = 2 * NCOMP * COMP_TILE;  // 48 KB
     static constexpr uint32_t IDESC = make_idesc(1, TILE_M, TILE_N);
+    static constexpr int KSTEP = 16;                 // k per BF16 MMA
 };
-template <> struct Cfg<MODE_TF32X3> {
-    static constexpr int NCOMP = 2;
+struct CfgTF32 {
+    static constexpr bool TF32 = true;
     static constexpr uint32_t ROW_BYTES = BK * 4;    // 128
     static constexpr uint32_t COMP_TILE = HALF * ROW_BYTES;         // 16 KB
-    static constexpr uint32_t SLICE_STAGE = 2 * NCOMP * COMP_TILE;  // 64 KB
     static constexpr uint32_t IDESC = make_idesc(2, TILE_M, TILE_N);
+    static constexpr int KSTEP = 8;                  // k per TF32 MMA
+};
+template <> struct Cfg<MODE_BF16X9> : CfgBF16 {
+    static constexpr int NPROD = 9;
+    __host__ __device__ static constexpr int pi(int p) { constexpr int v[9] = {2, 1, 2, 0, 1, 2, 0, 1, 0}; return v[p]; }
+    __host__ __device__ static constexpr int pj(int p) { constexpr int v[9] = {2, 2, 1, 2, 1, 0, 1, 0, 0}; return v[p]; }
+};
+template <> struct Cfg<MODE_BF16X6> : CfgBF16 {
+    static constexpr int NPROD = 6;
+    __host__ __device__ static constexpr int pi(int p) { constexpr int v[6] = {0, 1, 2, 0, 1, 0}; return v[p]; }
+    __host__ __device__ static constexpr int pj(int p) { constexpr int v[6] = {2, 1, 0, 1, 0, 0}; return v[p]; }
+};
+template <> struct Cfg<MODE_TF32X3> : CfgTF32 {
+    static constexpr int NCOMP = 2;
+    static constexpr uint32_t SLICE_STAGE = 2 * NCOMP * COMP_TILE;  // 64 KB
+    static constexpr int NPROD = 3;
+    __host__ __device__ static constexpr int pi(int p) { constexpr int v[3] = {1, 0, 0}; return v[p]; }
+    __host__ __device__ static constexpr int pj(int p) { constexpr int v[3] = {0, 1, 0}; return v[p]; }
+};
+template <> struct Cfg<MODE_TF32X1> : CfgTF32 {
+    static constexpr int NCOMP = 1;
+    static constexpr uint32_t SLICE_STAGE = 2 * NCOMP * COMP_TILE;  // 32 KB
+    static constexpr int NPROD = 1;
+    __host__ __device__ static constexpr int pi(int) { return 0; }
+    __host__ __device__ static constexpr int pj(int) { return 0; }
 };
 
 // Pipeline depths and output staging, chosen per launch.  Shared memory
@@ -98,8 +129,12 @@ template <> struct PipeCfg<MODE_BF16X9, PIPE_SHORT_K> {
 template <> struct PipeCfg<MODE_BF16X9, PIPE_LONG_K> {
     static constexpr int NF = 2, NS = 3, OUT_COLS = 16;
 };
+template <int PIPE> struct PipeCfg<MODE_BF16X6, PIPE> : PipeCfg<MODE_BF16X9, PIPE> {};
 template <int PIPE> struct PipeCfg<MODE_TF32X3, PIPE> {
     static constexpr int NF = 2, NS = 2, OUT_COLS = 32;
+};
+template <int PIPE> struct PipeCfg<MODE_TF32X1, PIPE> {
+    static constexpr int NF = 3, NS = 3, OUT_COLS = 32;
 };
 
 template <int MODE, int PIPE>
@@ -187,13 +222,20 @@ __device__ __forceinline__ void split_tf32x3_1(float x, uint32_t& hi, uint32_t& 
 template <int MODE>
 __device__ __forceinline__ void store_components(uint8_t* dst, uint32_t row, uint32_t g, const float (&x)[8]) {
     using C = Cfg<MODE>;
-    if constexpr (MODE == MODE_BF16X9) {
+    if constexpr (!C::TF32) {
         uint4 s0, s1, s2;
         split_bf16x9_8(x, s0, s1, s2);
         const uint32_t o = off_bf16_chunk(row, g);
         *reinterpret_cast<uint4*>(dst + o) = s0;
         *reinterpret_cast<uint4*>(dst + C::COMP_TILE + o) = s1;
         *reinterpret_cast<uint4*>(dst + 2 * C::COMP_TILE + o) = s2;
+    } else if constexpr (C::NCOMP == 1) {
+        uint32_t h[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[i] = tf32_rn_bits(__float_as_uint(x[i]));
+        const uint32_t o0 = off_f32_chunk(row, 2 * g), o1 = off_f32_chunk(row, 2 * g + 1);
+        *reinterpret_cast<uint4*>(dst + o0) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(dst + o1) = make_uint4(h[4], h[5], h[6], h[7]);
     } else {
         uint32_t h[8], l[8];
 #pragma unroll
@@ -239,37 +281,22 @@ __device__ __forceinline__ void split_operand(const uint8_t* src, uint8_t* dst, 
 }
 
 // Issue the pair products of one stage into TMEM accumulator `d`, starting
-// from zero.  BF16x9: bands 4, 3, 2, 1, 0 (i + j), each over the two K=16
-// steps of the stage.  TF32x3: lo*hi, hi*lo, hi*hi over four K=8 steps.
+// from zero: the mode's (i, j) component products, smallest first (BF16x9:
+// bands 4, 3, 2, 1, 0; TF32x3: lo*hi, hi*lo, hi*hi), each over the K steps of
+// the stage (two of 16 for BF16, four of 8 for TF32).
 template <int MODE>
 __device__ __forceinline__ void issue_stage_mmas(uint32_t d, uint32_t a_base, uint32_t b_base) {
     using C = Cfg<MODE>;
     uint32_t acc = 0;
-    if constexpr (MODE == MODE_BF16X9) {
-        constexpr int PI[9] = {2, 1, 2, 0, 1, 2, 0, 1, 0};  // (i, j), smallest band first
-        constexpr int PJ[9] = {2, 2, 1, 2, 1, 0, 1, 0, 0};
 #pragma unroll
-        for (int p = 0; p < 9; ++p) {
+    for (int p = 0; p < C::NPROD; ++p) {
 #pragma unroll
-            for (int ks = 0; ks < BK / 16; ++ks) {
-                const uint64_t ad = sdesc_kmajor(a_base + PI[p] * C::COMP_TILE + ks * 32, C::ROW_BYTES);
-                const uint64_t bd = sdesc_kmajor(b_base + PJ[p] * C::COMP_TILE + ks * 32, C::ROW_BYTES);
-                mma_bf16_pair(d, ad, bd, C::IDESC, acc);
-                acc = 1;
-            }
-        }
-    } else {
-        constexpr int PI[3] = {1, 0, 0};  // 0 = hi, 1 = lo
-        constexpr int PJ[3] = {0, 1, 0};
-#pragma unroll
-        for (int p = 0; p < 3; ++p) {
-#pragma unroll
-            for (int ks = 0; ks < BK / 8; ++ks) {
-                const uint64_t ad = sdesc_kmajor(a_base + PI[p] * C::COMP_TILE + ks * 32, C::ROW_BYTES);
-                const uint64_t bd = sdesc_kmajor(b_base + PJ[p] * C::COMP_TILE + ks * 32, C::ROW_BYTES);
-                mma_tf32_pair(d, ad, bd, C::IDESC, acc);
-                acc = 1;
-            }
+        for (int ks = 0; ks < BK / C::KSTEP; ++ks) {
+            const uint64_t ad = sdesc_kmajor(a_base + C::pi(p) * C::COMP_TILE + ks * 32, C::ROW_BYTES);
+            const uint64_t bd = sdesc_kmajor(b_base + C::pj(p) * C::COMP_TILE + ks * 32, C::ROW_BYTES);
+            if constexpr (C::TF32) mma_tf32_pair(d, ad, bd, C::IDESC, acc);
+            else mma_bf16_pair(d, ad, bd, C::IDESC, acc);
+            acc = 1;
         }
     }
 }

@@ -64,7 +64,12 @@ typedef struct CUstream_st *emu_stream_t;
 
 typedef enum {
     EMU_MODE_BF16X9 = 0, /* three BF16 components, nine products, five bands (Fig. 1) */
-    EMU_MODE_TF32X3 = 1  /* two TF32 components, three products (Fig. 2, Eq. 1) */
+    EMU_MODE_TF32X3 = 1, /* two TF32 components, three products (Fig. 2, Eq. 1) */
+    /* Comparators, faster and less accurate: */
+    EMU_MODE_TF32X1 = 2, /* one-pass TF32: hi(a) hi(b) only ("TF32x3 on Ampere GPUs": the one-pass
+                            mode whose force jitter and drift the blog reports); error up to
+                            2^-10 |a||b| per product */
+    EMU_MODE_BF16X6 = 3  /* BF16x9 without bands 3 and 4 (six products); error up to 2^-20 |a||b| */
 } emu_mode_t;
 
 typedef enum { EMU_OP_N = 0, EMU_OP_T = 1 } emu_op_t;

@@ -67,8 +67,11 @@ def lib():
             L.oracle_sgemm_f32.argtypes = gemm_head + [f32, P, i64, P, i64, f32, P, i64, P, P, i64, P]
             L.oracle_gemm_bf16x9.argtypes = gemm_head + [f32, P, i64, P, i64, f32, P, i64, P, i32, P, i64, P, P]
             L.oracle_gemm_tf32x3.argtypes = gemm_head + [f32, P, i64, P, i64, f32, P, i64, P, i32, P, i64, P, P]
+            L.oracle_gemm_bf16x6.argtypes = gemm_head + [f32, P, i64, P, i64, f32, P, i64, P, P, i64, P]
+            L.oracle_gemm_tf32x1.argtypes = gemm_head + [f32, P, i64, P, i64, f32, P, i64, P, P, i64, P]
             for name in ("oracle_gemm_f64", "oracle_gemm_absdenom_f64", "oracle_sgemm_f32",
-                         "oracle_gemm_bf16x9", "oracle_gemm_tf32x3", "oracle_num_threads"):
+                         "oracle_gemm_bf16x9", "oracle_gemm_tf32x3", "oracle_gemm_bf16x6",
+                         "oracle_gemm_tf32x1", "oracle_num_threads"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -88,7 +91,8 @@ class use_library:
         L = ctypes.CDLL(self.path)
         for name in ("oracle_split_bf16x9", "oracle_split_bf16x9_f32", "oracle_split_tf32x3",
                      "oracle_gemm_f64", "oracle_gemm_absdenom_f64", "oracle_sgemm_f32",
-                     "oracle_gemm_bf16x9", "oracle_gemm_tf32x3", "oracle_num_threads"):
+                     "oracle_gemm_bf16x9", "oracle_gemm_tf32x3", "oracle_gemm_bf16x6",
+                     "oracle_gemm_tf32x1", "oracle_num_threads"):
             f, g = getattr(L, name), getattr(self._saved, name)
             f.argtypes, f.restype = g.argtypes, g.restype
         _lib = L
@@ -255,12 +259,40 @@ def gemm_tf32x3(p: Problem, rows=None, variant: int = TF32X3_HI_RN, with_terms=F
     return (out, terms) if with_terms else out
 
 
+def gemm_bf16x6(p: Problem, rows=None):
+    """Comparator: BF16x9 without bands 3 and 4 (six products)."""
+    (h, lda, ldb), (r, nr) = p._head(), p._rows(rows)
+    out = np.empty((nr, p.N), np.float32)
+    cp, ldc = p._cold()
+    rc = lib().oracle_gemm_bf16x6(*h, p.alpha, _ptr(p.A), lda, _ptr(p.B), ldb, p.beta, cp, ldc,
+                                  _ptr(p.bias), _ptr(r), nr, _ptr(out))
+    if rc:
+        raise MemoryError("oracle_gemm_bf16x6")
+    return out
+
+
+def gemm_tf32x1(p: Problem, rows=None):
+    """Comparator: one-pass TF32 (hi(a) hi(b) only)."""
+    (h, lda, ldb), (r, nr) = p._head(), p._rows(rows)
+    out = np.empty((nr, p.N), np.float32)
+    cp, ldc = p._cold()
+    rc = lib().oracle_gemm_tf32x1(*h, p.alpha, _ptr(p.A), lda, _ptr(p.B), ldb, p.beta, cp, ldc,
+                                  _ptr(p.bias), _ptr(r), nr, _ptr(out))
+    if rc:
+        raise MemoryError("oracle_gemm_tf32x1")
+    return out
+
+
 def gemm_emulated(p: Problem, mode: str, rows=None):
-    """The oracle's emulated result for mode 'bf16x9' or 'tf32x3'."""
+    """The oracle's emulated result for mode 'bf16x9', 'tf32x3', 'bf16x6' or 'tf32x1'."""
     if mode == "bf16x9":
         return gemm_bf16x9(p, rows)
     if mode == "tf32x3":
         return gemm_tf32x3(p, rows)
+    if mode == "bf16x6":
+        return gemm_bf16x6(p, rows)
+    if mode == "tf32x1":
+        return gemm_tf32x1(p, rows)
     raise ValueError(mode)
 
 
@@ -283,7 +315,14 @@ def normwise_bound(mode: str, K: int) -> float:
 
     TF32x3 reads K as max(K, 2): dropping lo*lo (Eq. 1) and the two split
     residuals leave up to 2^-21 = 8u per product, so at K = 1 no TF32x3
-    result, the oracle's included, can meet 4u."""
+    result, the oracle's included, can meet 4u.
+    Comparators: BF16x6 drops bands 3-4 (at most 2^-20 of each |a b|):
+    2 K u + 2^-20; one-pass TF32 keeps 11 significant bits per operand (at
+    most 2^-10 of each |a b|): 2 K u + 2^-10."""
+    if mode == "bf16x6":
+        return 2.0 * max(int(K), 1) * U + 2.0 ** -20
+    if mode == "tf32x1":
+        return 2.0 * max(int(K), 1) * U + 2.0 ** -10
     k = max(int(K), 1) if mode == "bf16x9" else max(int(K), 2)
     return (2.0 if mode == "bf16x9" else 4.0) * k * U
 

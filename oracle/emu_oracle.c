@@ -356,6 +356,46 @@ ORACLE_API int oracle_gemm_bf16x9(int transA, int transB, int64_t M, int64_t N, 
     return 0;
 }
 
+/* BF16x6 (a comparator, not on the blog's pages): the same split and the same
+ * per-band FP32 sums as BF16x9, keeping only bands 0, 1 and 2 (six of the
+ * nine products; the four products of bands 3 and 4 are dropped).  Sums in
+ * k order, recombined smallest band first: acc = S_2 2^-16 + S_1 2^-8 + S_0. */
+ORACLE_API int oracle_gemm_bf16x6(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                                  float alpha, const float *A, int64_t lda,
+                                  const float *B, int64_t ldb,
+                                  float beta, const float *Cold, int64_t ldc,
+                                  const float *bias, const int64_t *rows, int64_t nrows, float *C)
+{
+    if (!rows) nrows = M;
+    float *pa = pack_opA(transA, M, K, A, lda);
+    float *pb = pack_opBt(transB, N, K, B, ldb);
+    float *sa = pa ? split3_planes(pa, M * K) : NULL;
+    float *sb = pb ? split3_planes(pb, N * K) : NULL;
+    if (!pa || !pb || !sa || !sb) { free(pa); free(pb); free(sa); free(sb); return -1; }
+    const int64_t MK = M * K, NK = N * K;
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t m = row_at(rows, r);
+        for (int64_t n = 0; n < N; ++n) {
+            const float *a[3] = { sa + m * K, sa + MK + m * K, sa + 2 * MK + m * K };
+            const float *b[3] = { sb + n * K, sb + NK + n * K, sb + 2 * NK + n * K };
+            float S[3] = { 0.0f, 0.0f, 0.0f };
+            for (int64_t k = 0; k < K; ++k)
+                for (int band = 0; band <= 2; ++band)
+                    for (int i = 0; i <= band; ++i) {
+                        int j = band - i;
+                        S[band] = S[band] + a[i][k] * b[j][k];
+                    }
+            float acc = S[2] * 0x1p-16f;
+            acc = acc + S[1] * 0x1p-8f;
+            acc = acc + S[0];
+            C[r * N + n] = epilogue_f32(acc, alpha, beta, Cold + m * ldc + n, bias ? bias + n : NULL);
+        }
+    }
+    free(pa); free(pb); free(sa); free(sb);
+    return 0;
+}
+
 /* ------------------------------------------------------------------------ */
 /* Steps 2-3: TF32x3                                                         */
 /* ------------------------------------------------------------------------ */
@@ -410,6 +450,36 @@ ORACLE_API int oracle_gemm_tf32x3(int transA, int transB, int64_t M, int64_t N, 
         }
     }
     free(pa); free(pb); free(ha); free(hb);
+    return 0;
+}
+
+/* One-pass TF32 ([Blog] "TF32x3 on Ampere GPUs": the faster, less accurate
+ * comparator): a b ~= hi(a) hi(b) with hi the nearest TF32 number, one FP32
+ * round-to-nearest sum over k.  Each product of two 11-bit significands is
+ * exact in FP32. */
+ORACLE_API int oracle_gemm_tf32x1(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                                  float alpha, const float *A, int64_t lda,
+                                  const float *B, int64_t ldb,
+                                  float beta, const float *Cold, int64_t ldc,
+                                  const float *bias, const int64_t *rows, int64_t nrows, float *C)
+{
+    if (!rows) nrows = M;
+    float *pa = pack_opA(transA, M, K, A, lda);
+    float *pb = pack_opBt(transB, N, K, B, ldb);
+    if (!pa || !pb) { free(pa); free(pb); return -1; }
+    for (int64_t i = 0; i < M * K; ++i) pa[i] = tf32_rn(pa[i]);
+    for (int64_t i = 0; i < N * K; ++i) pb[i] = tf32_rn(pb[i]);
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t m = row_at(rows, r);
+        for (int64_t n = 0; n < N; ++n) {
+            const float *ar = pa + m * K, *br = pb + n * K;
+            float acc = 0.0f;
+            for (int64_t k = 0; k < K; ++k) acc = acc + ar[k] * br[k];
+            C[r * N + n] = epilogue_f32(acc, alpha, beta, Cold + m * ldc + n, bias ? bias + n : NULL);
+        }
+    }
+    free(pa); free(pb);
     return 0;
 }
 

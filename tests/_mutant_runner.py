@@ -33,6 +33,11 @@ def run_pins():
     g.test_bf16x9_bands_hold_the_nine_products()
     g.test_tf32x3_terms_are_the_three_products()
     g.test_tf32x3_drops_lo_times_lo_closed_form()
+    g.test_bf16x6_keeps_bands_0_to_2_closed_form()
+    g.test_tf32x1_single_product_is_hi_times_hi()
+    g.test_tf32x1_closed_form_and_bound()
+    for tA, tB in g.TRANS:
+        g.test_bf16x6_against_exact_rationals(tA, tB)
     g.test_alpha_beta_bias_placement()
     g.test_beta_zero_never_reads_c()
     g.test_k_zero_gives_beta_c_plus_bias()

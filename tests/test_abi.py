@@ -46,7 +46,9 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_enums_match_binding():
     modes = _declared_enum("EMU_MODE_")
-    assert modes == {"EMU_MODE_BF16X9": emu.EMU_MODE_BF16X9, "EMU_MODE_TF32X3": emu.EMU_MODE_TF32X3}
+    assert modes == {"EMU_MODE_BF16X9": emu.EMU_MODE_BF16X9, "EMU_MODE_TF32X3": emu.EMU_MODE_TF32X3,
+                     "EMU_MODE_TF32X1": emu.EMU_MODE_TF32X1, "EMU_MODE_BF16X6": emu.EMU_MODE_BF16X6}
+    assert {f"EMU_MODE_{k.upper()}": v for k, v in emu.MODES.items()} == modes
     ops = _declared_enum("EMU_OP_")
     assert ops == {"EMU_OP_N": emu.EMU_OP_N, "EMU_OP_T": emu.EMU_OP_T}
     st = _declared_enum("EMU_STATUS_")

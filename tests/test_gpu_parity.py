@@ -211,3 +211,31 @@ def test_emu_linear_module_matches_fp32_layer():
         assert float((x.grad.double().cpu() - xr.grad).abs().max()) <= 1e-5 * scale(xr.grad)
         assert float((lin.weight.grad.double().cpu() - ref.weight.grad).abs().max()) <= 1e-5 * scale(ref.weight.grad)
         assert float((lin.bias.grad.double().cpu() - ref.bias.grad).abs().max()) <= 1e-5 * scale(ref.bias.grad)
+
+
+@pytest.mark.parametrize("mode", ["tf32x1", "bf16x6"])
+def test_comparator_modes(mode):
+    """The comparators (one-pass TF32, BF16x6) against their oracles: the
+    tiny config with beta, a ragged problem in every storage order, and the
+    PET-small forward and input gradient on a row sample."""
+    import fp32_emulated_gemm_gb300 as emu
+    A, B, Cold = W.tiny_inputs()
+    C = _gpu.gpu_sgemm(mode, A, B, beta=1.0, C_old=Cold)
+    _gpu.compare(mode, C, oracle.Problem(A, B, beta=1.0, C_old=Cold))
+    rng = np.random.default_rng(8)
+    M, N, K = 300, 260, 200
+    A_op = rng.standard_normal((M, K)).astype(np.float32)
+    B_op = rng.standard_normal((K, N)).astype(np.float32)
+    for tA, tB in [(False, False), (True, False), (False, True), (True, True)]:
+        Am = np.ascontiguousarray(A_op.T) if tA else A_op
+        Bm = np.ascontiguousarray(B_op.T) if tB else B_op
+        C = _gpu.gpu_sgemm(mode, Am, Bm, transA=tA, transB=tB)
+        _gpu.compare(mode, C, oracle.Problem(Am, Bm, transA=tA, transB=tB))
+    s = W.PET_SMALL
+    X, Wt, b, dY = W.linear_inputs(s, W.CONFIG_ID["pet_small"])
+    rows = W.sample_rows(s.M, every=32, edge=64)
+    Y = emu.linear_fwd(_gpu.to_dev(X), _gpu.to_dev(Wt), _gpu.to_dev(b), mode=mode)
+    dX = emu.linear_bwd_input(_gpu.to_dev(dY), _gpu.to_dev(Wt), mode=mode)
+    assert emu.emu_stream_check() == 0
+    _gpu.compare(mode, Y.cpu().numpy(), oracle.Problem(X, Wt, transB=True, bias=b), rows)
+    _gpu.compare(mode, dX.cpu().numpy(), oracle.Problem(dY, Wt), rows)

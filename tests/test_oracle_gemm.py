@@ -208,6 +208,57 @@ def test_tf32x3_single_product_error_floor():
     assert rel_bf.max() <= oracle.normwise_bound("bf16x9", 1)
 
 
+# ----------------------------------------------------- comparator modes ----
+def test_bf16x6_keeps_bands_0_to_2_closed_form():
+    """a = b = 1 + 2^-8 + 2^-16 has components (1, 1, 1), so the band sums are
+    S = (1, 2, 3, 2, 1).  BF16x6 keeps bands 0-2: 1 + 2^-7 + 3 2^-16 exactly;
+    BF16x9 adds 2 2^-24 + 2^-32, which rounds to one more ulp (2^-23)."""
+    a = np.array([[1 + 2.0 ** -8 + 2.0 ** -16]], np.float32)
+    p = oracle.Problem(a, a)
+    assert oracle.gemm_bf16x6(p)[0, 0] == np.float32(1 + 2.0 ** -7 + 3 * 2.0 ** -16)
+    assert oracle.gemm_bf16x9(p)[0, 0] == np.float32(1 + 2.0 ** -7 + 3 * 2.0 ** -16 + 2.0 ** -23)
+
+
+@pytest.mark.parametrize("tA,tB", TRANS)
+def test_bf16x6_against_exact_rationals(tA, tB):
+    rng = np.random.default_rng(22)
+    for (M, N, K) in [(3, 3, 1), (4, 5, 8), (3, 4, 24)]:
+        A_op = _bits.random_bits_matrix(rng, (M, K), -12, 12)
+        B_op = _bits.random_bits_matrix(rng, (K, N), -12, 12)
+        A, B = _layout(A_op, B_op, tA, tB)
+        C = oracle.gemm_bf16x6(oracle.Problem(A, B, transA=tA, transB=tB))
+        err = _rel_err_vs_exact(C, _bits.exact_gemm(A_op, B_op), _bits.exact_absgemm(A_op, B_op))
+        # three FP32 band sums + recombination, plus the dropped bands 3-4
+        # (each |c_i c_j| 2^-8(i+j) < 4 2^-24 |a b|): (K + 2) u + 2^-20
+        assert err <= (K + 2) * U + 2.0 ** -20
+        assert err <= oracle.normwise_bound("bf16x6", K)
+
+
+def test_tf32x1_single_product_is_hi_times_hi():
+    """One-pass TF32 at K = 1 is hi(a) hi(b) exactly (11-bit significands)."""
+    rng = np.random.default_rng(23)
+    a = _bits.random_bits_matrix(rng, (50, 1), -20, 20)
+    b = _bits.random_bits_matrix(rng, (1, 40), -20, 20)
+    C = oracle.gemm_tf32x1(oracle.Problem(a, b))
+    ha, _ = oracle.split_tf32x3(a.ravel())
+    hb, _ = oracle.split_tf32x3(b.ravel())
+    assert np.array_equal(C.astype(np.float64), np.outer(ha.astype(np.float64), hb.astype(np.float64)))
+
+
+def test_tf32x1_closed_form_and_bound():
+    """a = b = 1 + 2^-11 + 2^-12 rounds to hi = 1 + 2^-10, so one-pass TF32
+    gives (1 + 2^-10)^2 = 1 + 2^-9 + 2^-20; random data stays inside
+    2 K u + 2^-10 of the exact product sum."""
+    a = np.array([[1 + 2.0 ** -11 + 2.0 ** -12]], np.float32)
+    assert oracle.gemm_tf32x1(oracle.Problem(a, a))[0, 0] == np.float32(1 + 2.0 ** -9 + 2.0 ** -20)
+    rng = np.random.default_rng(24)
+    A = _bits.random_bits_matrix(rng, (4, 24), -12, 12)
+    B = _bits.random_bits_matrix(rng, (24, 5), -12, 12)
+    C = oracle.gemm_tf32x1(oracle.Problem(A, B))
+    err = _rel_err_vs_exact(C, _bits.exact_gemm(A, B), _bits.exact_absgemm(A, B))
+    assert 2.0 ** -16 < err <= oracle.normwise_bound("tf32x1", 24)
+
+
 # ------------------------------------------- closed forms (all variants) ----
 def _all_modes(p):
     return {

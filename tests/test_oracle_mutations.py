@@ -39,6 +39,10 @@ MUTANTS = {
     "sgemm_first_term_dropped": ("acc = fmaf(ar[k], br[k], acc);",
                                  "acc = (k == 0) ? 0.0f : fmaf(ar[k], br[k], acc);"),
     "bias_dropped": ("if (bias_elem) c = c + *bias_elem;", ";"),
+    "bf16x6_band1_scale": ("            acc = acc + S[1] * 0x1p-8f;\n            acc = acc + S[0];",
+                           "            acc = acc + S[1] * 0x1p-7f;\n            acc = acc + S[0];"),
+    "tf32x1_truncates": ("for (int64_t i = 0; i < M * K; ++i) pa[i] = tf32_rn(pa[i]);",
+                         "for (int64_t i = 0; i < M * K; ++i) pa[i] = tf32_rz(pa[i]);"),
 }
 
 
