@@ -380,7 +380,8 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         tmem_relinquish_pair();
     }
     tc_fence_before();
-    cluster_sync();  // barriers of both CTAs initialised, TMEM of both allocated
+    __syncthreads();          // this CTA's barriers and TMEM address visible to all its threads
+    cluster_sync_relaxed();   // the peer's barriers initialised before any arrival on them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const uint64_t budget = p.wait_budget_ns;
@@ -425,8 +426,8 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
             for (int u = cid; ok && u < p.num_units; u += ncl) {
                 const Unit w = unit_of(p, u);
                 for (int ks = w.kb; ks < w.ke; ++ks) {
-                    if (!mbar_wait_cluster(&acc_empty[b], bph ^ 1u, abort_flag, budget, 2)) { ok = false; break; }
-                    if (!mbar_wait_cluster(&slice_full[s], ph, abort_flag, budget, 2)) { ok = false; break; }
+                    if (!mbar_wait(&acc_empty[b], bph ^ 1u, abort_flag, budget, 2)) { ok = false; break; }
+                    if (!mbar_wait(&slice_full[s], ph, abort_flag, budget, 2)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_base = slice_base + s * C::SLICE_STAGE;
                     const uint32_t b_base = a_base + C::NCOMP * C::COMP_TILE;

@@ -57,25 +57,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return done != 0;
 }
 
-// Same, with acquire at cluster scope (arrivals come from the peer CTA too).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-// Arrive (release, cluster scope) on the barrier at the same shared-memory
-// offset in CTA `rank` of this cluster.
+// Arrive on the barrier at the same shared-memory offset in CTA `rank` of
+// this cluster.  What such an arrival publishes (components in the arriving
+// CTA's own shared memory, made visible to the tensor cores by a proxy fence;
+// TMEM reads finished with tcgen05.wait::ld) needs only CTA-scope release
+// ordering.  A cluster-scope release waits for the SM's outstanding memory
+// traffic and measured 1-2 thousand cycles per arrival on this kernel.
 __device__ __forceinline__ void mbar_arrive_cluster(uint64_t* bar, uint32_t rank) {
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(bar)), "r"(rank));
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+    asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -97,6 +88,12 @@ __device__ __forceinline__ uint32_t num_clusters_x() {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Cluster barrier without release ordering on the arrive side: enough where
+// the only cross-CTA fact to publish is barrier initialisation, which
+// fence.mbarrier_init orders by itself.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
 // Wait for the phase of `bar` with the given parity to complete.  Returns
 // false, without waiting further, when *abort is set by another warp or when
@@ -107,24 +104,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 15u) == 0) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > budget_ns) {
-                atomicOr(&g_error_flag, ERR_TIMEOUT | (role << 8));
-                *abort = 1;
-                return false;
-            }
-        }
-    }
-}
-
-// Single-thread wait with cluster-scope acquire.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                  uint64_t budget_ns, unsigned role) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
         if ((i & 15u) == 0) {
             if (*abort) return false;
             if (globaltimer_ns() - t0 > budget_ns) {
