@@ -173,11 +173,13 @@ bool encode_f32_2d(CUtensorMap* map, const float* base, uint64_t inner, uint64_t
     return r == CUDA_SUCCESS;
 }
 
-// op(X) tile map: K-major operands (rows of K) load {32 k, 128 rows};
-// MN-major operands (rows of MN) load four {32 mn, 32 k} boxes.
-bool encode_operand(CUtensorMap* map, const float* X, bool mn_major, int64_t MN, int64_t K, int64_t ld) {
+// op(X) tile map for tiles of `rows` rows (128 for op(A), TN / 2 for op(B)):
+// K-major operands (rows of K) load one {32 k, rows} box; MN-major operands
+// (rows of MN) load rows / 32 boxes of {32 mn, 32 k}.
+bool encode_operand(CUtensorMap* map, const float* X, bool mn_major, int64_t MN, int64_t K, int64_t ld,
+                    uint32_t rows) {
     // TMA needs every extent >= 1; a zero extent never reaches here.
-    if (!mn_major) return encode_f32_2d(map, X, (uint64_t)K, (uint64_t)MN, (uint64_t)ld, BK, HALF);
+    if (!mn_major) return encode_f32_2d(map, X, (uint64_t)K, (uint64_t)MN, (uint64_t)ld, BK, rows);
     return encode_f32_2d(map, X, (uint64_t)MN, (uint64_t)K, (uint64_t)ld, 32, BK);
 }
 
@@ -243,29 +245,62 @@ emu_status_t workspace_for(int dev, cudaStream_t stream, size_t floats, size_t c
     return EMU_STATUS_SUCCESS;
 }
 
-// Pieces per tile.  Cost model in units of one pipeline stage (measured on
-// GB300): every unit pays its k-stages plus about 3 stages of output stores
-// (final tile or partial); a split tile's last piece also re-reads the other
-// pieces' partials (about 1.5 stages each) and stores the final tile.  Units
-// run in waves over the resident CTA pairs.
-int choose_split_k(int tiles, int k_stages, int pairs) {
-    const char* env = std::getenv("EMU_SPLIT_K");
-    if (env) {
-        const int v = std::atoi(env);
-        if (v >= 1) return v < k_stages ? v : k_stages;
+// The launch plan: pipeline shape, tiles and pieces per tile.
+struct Plan {
+    int pipe;       // PIPE_SHORT_K or PIPE_LONG_K
+    int tn;         // pair tile width
+    int tiles_m, tiles_n, num_tiles, k_stages, split_k;
+};
+
+// Long k-loops per work unit favour three component stages; short ones the
+// wider output staging (see PipeCfg).
+constexpr int kLongKMinStages = 16;
+
+// Cost of a plan in units of one pipeline stage (measured on GB300): every
+// work unit pays its k-stages plus about 3 stages of output stores (final
+// tile or partial), which the two TMEM accumulators cannot hide; a split
+// tile's last piece also re-reads the other pieces' partials (about 1.5
+// stages each) and stores the final tile.  Units run in waves over the
+// resident CTA pairs.
+double plan_cost(long long tiles, int k_stages, int S, int pairs) {
+    const long long units = tiles * S;
+    const long long waves = (units + pairs - 1) / pairs;
+    const long long per = (k_stages + S - 1) / S;
+    double cost = (double)waves * (double)(per + 3);
+    if (S > 1) cost += 1.5 * (S - 1) + 3.0;
+    return cost;
+}
+
+int env_int(const char* name, int dflt) {
+    const char* v = std::getenv(name);
+    return v ? std::atoi(v) : dflt;
+}
+
+// EMU_SPLIT_K and EMU_PIPE (0 short-k, 1 long-k) override the choice, for
+// diagnostics and tuning.
+Plan make_plan(int64_t M, int64_t N, int64_t K, int pairs) {
+    Plan plan{};
+    plan.tn = 256;
+    plan.tiles_m = (int)((M + TILE_M - 1) / TILE_M);
+    plan.tiles_n = (int)((N + plan.tn - 1) / plan.tn);
+    plan.num_tiles = plan.tiles_m * plan.tiles_n;
+    plan.k_stages = (int)((K + BK - 1) / BK);
+    const int force_split = env_int("EMU_SPLIT_K", 0);
+    if (force_split >= 1) {
+        plan.split_k = force_split < plan.k_stages ? force_split : plan.k_stages;
+    } else {
+        double best_cost = -1.0;
+        for (int S = 1; S <= 64 && S <= plan.k_stages; ++S) {
+            if (S > 1 && plan.k_stages / S < 2) break;
+            const double cost = plan_cost(plan.num_tiles, plan.k_stages, S, pairs);
+            if (best_cost < 0 || cost < best_cost - 1e-9) { best_cost = cost; plan.split_k = S; }
+        }
     }
-    int best = 1;
-    double best_cost = -1.0;
-    for (int S = 1; S <= 64 && S <= k_stages; ++S) {
-        if (S > 1 && k_stages / S < 2) break;
-        const long long units = (long long)tiles * S;
-        const long long waves = (units + pairs - 1) / pairs;
-        const long long per = (k_stages + S - 1) / S;
-        double cost = (double)waves * (double)(per + 3);
-        if (S > 1) cost += 1.5 * (S - 1) + 3.0;
-        if (best_cost < 0 || cost < best_cost - 1e-9) { best_cost = cost; best = S; }
-    }
-    return best;
+    const int per_unit = (plan.k_stages + plan.split_k - 1) / plan.split_k;
+    const int force_pipe = env_int("EMU_PIPE", -1);
+    plan.pipe = force_pipe == PIPE_SHORT_K || force_pipe == PIPE_LONG_K ? force_pipe
+              : per_unit >= kLongKMinStages ? PIPE_LONG_K : PIPE_SHORT_K;
+    return plan;
 }
 
 unsigned long long wait_budget_ns() {
@@ -277,10 +312,6 @@ unsigned long long wait_budget_ns() {
     return v;
 }
 
-// Long k-loops per work unit favour three component stages; short ones the
-// wider output staging (see PipeCfg).
-constexpr int kLongKMinStages = 16;
-
 template <int MODE, int PIPE>
 cudaError_t launch_one(cudaLaunchConfig_t cfg, const Params& p) {
     cfg.dynamicSmemBytes = smem_bytes<MODE, PIPE>();
@@ -289,13 +320,27 @@ cudaError_t launch_one(cudaLaunchConfig_t cfg, const Params& p) {
 
 // The launch's own status (cudaLaunchKernelEx), so that an error left by an
 // unrelated earlier runtime call on this host thread is not reported as ours.
-cudaError_t launch_gemm(emu_mode_t mode, const Params& p, int clusters, cudaStream_t stream) {
+// Programmatic dependent launch (EMU_PDL=0 turns it off): the kernel may be
+// scheduled while the previous kernel in the stream finishes; it runs its
+// set-up and then waits for that kernel before touching global memory.
+bool pdl_enabled() {
+    static const bool v = env_int("EMU_PDL", 1) != 0;
+    return v;
+}
+
+cudaError_t launch_gemm(emu_mode_t mode, int pipe, const Params& p, int clusters, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
     cfg.stream = stream;
-    const int per_unit = (p.k_stages + p.split_k - 1) / p.split_k;
-    const bool long_k = per_unit >= kLongKMinStages;
+    cudaLaunchAttribute attr[1];
+    if (pdl_enabled()) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    const bool long_k = pipe == PIPE_LONG_K;
     cudaError_t e;
     switch (mode) {
         case EMU_MODE_TF32X3: e = launch_one<MODE_TF32X3, PIPE_SHORT_K>(cfg, p); break;
@@ -347,17 +392,19 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
         return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
     }
 
+    const int pairs = dev->max_clusters[mode == EMU_MODE_TF32X3 ? 1 : 0];
+    const Plan plan = make_plan(M, N, K, pairs);
     Params p{};
-    if (!encode_operand(&p.tmA, A, a_mn, M, K, lda) || !encode_operand(&p.tmB, B, b_mn, N, K, ldb))
+    if (!encode_operand(&p.tmA, A, a_mn, M, K, lda, HALF) ||
+        !encode_operand(&p.tmB, B, b_mn, N, K, ldb, (uint32_t)plan.tn / 2))
         return EMU_STATUS_LAUNCH_FAILED;
     p.M = (int)M; p.N = (int)N; p.K = (int)K;
     p.a_mn_major = a_mn; p.b_mn_major = b_mn;
-    p.tiles_m = (int)((M + TILE_M - 1) / TILE_M);
-    p.tiles_n = (int)((N + TILE_N - 1) / TILE_N);
-    p.num_tiles = p.tiles_m * p.tiles_n;
-    p.k_stages = (int)((K + BK - 1) / BK);
-    const int pairs = dev->max_clusters[mode == EMU_MODE_TF32X3 ? 1 : 0];
-    p.split_k = choose_split_k(p.num_tiles, p.k_stages, pairs);
+    p.tiles_m = plan.tiles_m;
+    p.tiles_n = plan.tiles_n;
+    p.num_tiles = plan.num_tiles;
+    p.k_stages = plan.k_stages;
+    p.split_k = plan.split_k;
     p.num_units = p.num_tiles * p.split_k;
     p.alpha = alpha; p.beta = beta;
     p.c_old = C; p.c = C; p.ldc = ldc;
@@ -367,7 +414,7 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
         int devid = 0;
         cudaGetDevice(&devid);
         Workspace* w = nullptr;
-        const size_t floats = (size_t)p.num_tiles * p.split_k * TILE_M * TILE_N;
+        const size_t floats = (size_t)p.num_tiles * p.split_k * TILE_M * plan.tn;
         st = workspace_for(devid, stream, floats, (size_t)p.num_tiles * 2, &w);
         if (st != EMU_STATUS_SUCCESS) return st;
         p.workspace = w->partials;
@@ -375,42 +422,45 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
     }
     const int clusters = p.num_units < pairs ? p.num_units : pairs;
     if (log_enabled())
-        std::fprintf(stderr, "[emu] %s M=%lld N=%lld K=%lld a_mn=%d b_mn=%d tiles=%dx%d k_stages=%d split_k=%d "
-                             "units=%d pairs=%d (max %d) long_k_pipe=%u\n",
-                     mode_name(mode), (long long)M, (long long)N, (long long)K,
-                     (int)a_mn, (int)b_mn, p.tiles_m, p.tiles_n, p.k_stages, p.split_k, p.num_units, clusters,
-                     pairs, (p.k_stages + p.split_k - 1) / p.split_k >= kLongKMinStages ? 1u : 0u);
-    return launch_gemm(mode, p, clusters, stream) == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
+        std::fprintf(stderr, "[emu] %s M=%lld N=%lld K=%lld a_mn=%d b_mn=%d pipe=%d tile=256x%d tiles=%dx%d "
+                             "k_stages=%d split_k=%d units=%d pairs=%d (max %d)\n",
+                     mode_name(mode), (long long)M, (long long)N, (long long)K, (int)a_mn, (int)b_mn, plan.pipe,
+                     plan.tn, p.tiles_m, p.tiles_n, p.k_stages, p.split_k, p.num_units, clusters, pairs);
+    return launch_gemm(mode, plan.pipe, p, clusters, stream) == cudaSuccess ? EMU_STATUS_SUCCESS
+                                                                             : EMU_STATUS_LAUNCH_FAILED;
 }
 
 // ----------------------------------------------------------- split dump ----
-template <int MODE>
+// One tile of ROWS rows (128: the op(A) tile; 64: the op(B) tile of TN = 128
+// plans) through the kernel's split.
+template <int MODE, int ROWS>
 __global__ void __launch_bounds__(256, 1) split_dump_kernel(const __grid_constant__ CUtensorMap tm, int R, int Kc,
                                                             int mn_major, void* out) {
     using C = Cfg<MODE>;
+    constexpr uint32_t F32_BYTES = ROWS * BK * 4, COMP = ROWS * C::ROW_BYTES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* f32 = smem;
-    uint8_t* comp = smem + FP32_TILE_BYTES;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(comp + C::NCOMP * C::COMP_TILE);
+    uint8_t* comp = smem + F32_BYTES;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(comp + C::NCOMP * COMP);
     if (threadIdx.x == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(bar, FP32_TILE_BYTES);
+        mbar_arrive_expect_tx(bar, F32_BYTES);
         if (!mn_major) tma_load_2d(f32, &tm, bar, 0, 0);
-        else for (int j = 0; j < 4; ++j) tma_load_2d(f32 + j * 4096, &tm, bar, 32 * j, 0);
+        else for (int j = 0; j < ROWS / 32; ++j) tma_load_2d(f32 + j * 4096, &tm, bar, 32 * j, 0);
     }
     volatile int no_abort = 0;
     if (!mbar_wait_warp(bar, 0, &no_abort, 1000000000ull, 5)) return;
-    split_operand<MODE, 256>(f32, comp, mn_major != 0, threadIdx.x);
+    split_operand<MODE, 256, ROWS>(f32, comp, mn_major != 0, threadIdx.x);
     __syncthreads();
     for (int i = threadIdx.x; i < R * Kc; i += blockDim.x) {
         const uint32_t r = i / Kc, k = i % Kc;
         for (int c = 0; c < C::NCOMP; ++c) {
-            const uint8_t* tile = comp + c * C::COMP_TILE;
+            const uint8_t* tile = comp + c * COMP;
             if constexpr (MODE == MODE_BF16X9) {
                 const uint16_t v = *reinterpret_cast<const uint16_t*>(tile + off_bf16_chunk(r, k >> 3) + (k & 7u) * 2);
                 reinterpret_cast<uint16_t*>(out)[(size_t)c * R * Kc + i] = v;
@@ -508,20 +558,28 @@ emu_status_t emu_split_dump(emu_mode_t mode, int64_t R, int64_t Kc, const float*
     DeviceInfo* dev = nullptr;
     emu_status_t st = device_info(&dev);
     if (st != EMU_STATUS_SUCCESS) return st;
+    const bool rows64 = R <= 64;
     CUtensorMap tm;
-    if (!encode_operand(&tm, X, mn_major != 0, R, Kc, ldx)) return EMU_STATUS_LAUNCH_FAILED;
+    if (!encode_operand(&tm, X, mn_major != 0, R, Kc, ldx, rows64 ? 64u : (uint32_t)HALF))
+        return EMU_STATUS_LAUNCH_FAILED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int R32 = (int)R, K32 = (int)Kc;
+    // shared memory: FP32 tile, the components, the barrier, alignment slack
+    const uint32_t rows = rows64 ? 64u : (uint32_t)HALF;
+    const uint32_t bytes = mode == EMU_MODE_BF16X9
+        ? 1024 + rows * BK * 4 + 3 * rows * Cfg<MODE_BF16X9>::ROW_BYTES + 64
+        : 1024 + rows * BK * 4 + 2 * rows * Cfg<MODE_TF32X3>::ROW_BYTES + 64;
+    auto run = [&](auto kernel) {
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        cudaGetLastError();
+        kernel<<<1, 256, bytes, s>>>(tm, R32, K32, mn_major, out);
+    };
     if (mode == EMU_MODE_BF16X9) {
-        const uint32_t bytes = 1024 + FP32_TILE_BYTES + 3 * Cfg<MODE_BF16X9>::COMP_TILE + 64;
-        cudaFuncSetAttribute(split_dump_kernel<MODE_BF16X9>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        cudaGetLastError();
-        split_dump_kernel<MODE_BF16X9><<<1, 256, bytes, s>>>(tm, R32, K32, mn_major, out);
+        if (rows64) run(split_dump_kernel<MODE_BF16X9, 64>);
+        else run(split_dump_kernel<MODE_BF16X9, HALF>);
     } else {
-        const uint32_t bytes = 1024 + FP32_TILE_BYTES + 2 * Cfg<MODE_TF32X3>::COMP_TILE + 64;
-        cudaFuncSetAttribute(split_dump_kernel<MODE_TF32X3>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-        cudaGetLastError();
-        split_dump_kernel<MODE_TF32X3><<<1, 256, bytes, s>>>(tm, R32, K32, mn_major, out);
+        if (rows64) run(split_dump_kernel<MODE_TF32X3, 64>);
+        else run(split_dump_kernel<MODE_TF32X3, HALF>);
     }
     return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
 }
@@ -613,17 +671,19 @@ emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, 
         return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
     }
 
+    const int pairs = dev->max_clusters[mode == EMU_MODE_TF32X3 ? 1 : 0];
+    const Plan plan = make_plan(M, N, K, pairs);
     Params p{};
-    if (!encode_operand(&p.tmA, A, a_mn, M, K, lda) || !encode_operand(&p.tmB, B, b_mn, N, K, ldb))
+    if (!encode_operand(&p.tmA, A, a_mn, M, K, lda, HALF) ||
+        !encode_operand(&p.tmB, B, b_mn, N, K, ldb, (uint32_t)plan.tn / 2))
         return EMU_STATUS_LAUNCH_FAILED;
     p.M = (int)M; p.N = (int)N; p.K = (int)K;
     p.a_mn_major = a_mn; p.b_mn_major = b_mn;
-    p.tiles_m = (int)((M + TILE_M - 1) / TILE_M);
-    p.tiles_n = (int)((N + TILE_N - 1) / TILE_N);
-    p.num_tiles = p.tiles_m * p.tiles_n;
-    p.k_stages = (int)((K + BK - 1) / BK);
-    const int pairs = dev->max_clusters[mode == EMU_MODE_TF32X3 ? 1 : 0];
-    p.split_k = choose_split_k(p.num_tiles, p.k_stages, pairs);
+    p.tiles_m = plan.tiles_m;
+    p.tiles_n = plan.tiles_n;
+    p.num_tiles = plan.num_tiles;
+    p.k_stages = plan.k_stages;
+    p.split_k = plan.split_k;
     p.num_units = p.num_tiles * p.split_k;
     p.alpha = alpha; p.beta = beta;
     p.c_old = C; p.c = C; p.ldc = ldc;
@@ -631,7 +691,7 @@ emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, 
     p.wait_budget_ns = wait_budget_ns();
     if (p.split_k > 1) {
         // partial tiles first, then one counter per CTA half-tile
-        const size_t partial_bytes = (size_t)p.num_tiles * p.split_k * TILE_M * TILE_N * sizeof(float);
+        const size_t partial_bytes = (size_t)p.num_tiles * p.split_k * TILE_M * plan.tn * sizeof(float);
         const size_t counter_off = (partial_bytes + 255) & ~size_t(255);
         const size_t counter_bytes = (size_t)p.num_tiles * 2 * sizeof(int);
         if (counter_off + counter_bytes > kNoAllocScratchBytes) return EMU_STATUS_NOT_SUPPORTED;
@@ -644,7 +704,8 @@ emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, 
         }
     }
     const int clusters = p.num_units < pairs ? p.num_units : pairs;
-    return launch_gemm(mode, p, clusters, stream) == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
+    return launch_gemm(mode, plan.pipe, p, clusters, stream) == cudaSuccess ? EMU_STATUS_SUCCESS
+                                                                             : EMU_STATUS_LAUNCH_FAILED;
 }
 
 }  // namespace

@@ -8,12 +8,12 @@
 // FP32 (BF16x9: along five anti-diagonal bands; TF32x3: Eq. 1, lo*lo dropped).
 //
 // One persistent kernel on CTA pairs (clusters of 2, one CTA per SM).  A pair
-// computes a 256 x 256 tile of C with 2-SM tensor-core MMAs (cta_group::2):
-// CTA r of the pair holds rows [128r, 128r+128) of the tile's op(A) block and
-// rows [128r, 128r+128) of its op(B)^T block; each SM's tensor core reads its
-// own A half and both B halves, and writes its 128 x 256 quarter of the
-// accumulator to its own TMEM.  Per CTA (16 warps):
-//   warp 0      TMA producer: FP32 tiles (128 x 32 of op(A), 128 x 32 of
+// computes a 256 x TN tile of C (TN = 256 or 128) with 2-SM tensor-core MMAs
+// (cta_group::2): CTA r of the pair holds rows [128r, 128r+128) of the
+// tile's op(A) block and rows [r TN/2, (r+1) TN/2) of its op(B)^T block; each
+// SM's tensor core reads its own A half and both B halves, and writes its
+// 128 x TN half of the accumulator to its own TMEM.  Per CTA (16 warps):
+//   warp 0      TMA producer: FP32 tiles (128 x 32 of op(A), TN/2 x 32 of
 //               op(B)) into a ring of shared-memory stages, zero fill beyond
 //               the matrix edges.
 //   warp 1      TMEM owner; in the leader CTA also the MMA issuer: for every
@@ -51,8 +51,7 @@ namespace emu {
 enum Mode : int { MODE_BF16X9 = 0, MODE_TF32X3 = 1, MODE_TF32X1 = 2, MODE_BF16X6 = 3 };
 
 constexpr int TILE_M = 256;       // rows of a pair tile (128 per CTA)
-constexpr int TILE_N = 256;       // columns of a pair tile (TMEM columns per accumulator)
-constexpr int HALF = 128;         // rows of op(A) and of op(B)^T held by one CTA
+constexpr int HALF = 128;         // rows of op(A) held by one CTA (= TMEM lanes)
 constexpr int BK = 32;            // k-values per pipeline stage
 constexpr int NUM_THREADS = 512;
 constexpr int WARP_PRODUCER = 0;
@@ -62,32 +61,31 @@ constexpr int NUM_SPLIT_WARPS = 6;
 constexpr int NUM_SPLIT_THREADS = NUM_SPLIT_WARPS * 32;
 constexpr int WARP_EPI0 = 8;
 constexpr int NUM_EPI_WARPS = 8;
-constexpr uint32_t TMEM_COLS = 2 * TILE_N;  // two accumulators, double-buffered (all 512)
+constexpr uint32_t TMEM_COLS = 512;         // all of TMEM: 512 / TN accumulators of TN columns
 constexpr uint32_t EPI_BARRIER = 1;         // named barrier of the 256 epilogue threads
 constexpr uint32_t SPLIT_BARRIER = 2;       // named barrier of the split threads
 
-// FP32 stage of one CTA: its op(A) half-tile then its op(B) half-tile.
+// FP32 op(A) half-tile of one CTA and stage (its op(B) part follows it).
 constexpr uint32_t FP32_TILE_BYTES = HALF * BK * 4;           // 16 KB
-constexpr uint32_t FP32_STAGE_BYTES = 2 * FP32_TILE_BYTES;    // 32 KB
 
-// Per mode: components per operand, their tile geometry, the MMA kind and
+// Per mode: components per operand, their row geometry, the MMA kind and
 // the (i, j) component products of a stage, smallest first (for BF16: band
-// i + j descending; for TF32: 0 = hi, 1 = lo).
+// i + j descending; for TF32: 0 = hi, 1 = lo).  COMP_TILE is one component
+// of the op(A) half-tile (128 rows).
 template <int MODE> struct Cfg;
 struct CfgBF16 {
     static constexpr bool TF32 = false;
     static constexpr int NCOMP = 3;                  // components per operand
     static constexpr uint32_t ROW_BYTES = BK * 2;    // 64: one BF16 row of a stage
     static constexpr uint32_t COMP_TILE = HALF * ROW_BYTES;         // 8 KB
-    static constexpr uint32_t SLICE_STAGE = 2 * NCOMP * COMP_TILE;  // 48 KB
-    static constexpr uint32_t IDESC = make_idesc(1, TILE_M, TILE_N);
+    static constexpr int KIND = 1;                   // instruction-descriptor operand format
     static constexpr int KSTEP = 16;                 // k per BF16 MMA
 };
 struct CfgTF32 {
     static constexpr bool TF32 = true;
     static constexpr uint32_t ROW_BYTES = BK * 4;    // 128
     static constexpr uint32_t COMP_TILE = HALF * ROW_BYTES;         // 16 KB
-    static constexpr uint32_t IDESC = make_idesc(2, TILE_M, TILE_N);
+    static constexpr int KIND = 2;
     static constexpr int KSTEP = 8;                  // k per TF32 MMA
 };
 template <> struct Cfg<MODE_BF16X9> : CfgBF16 {
@@ -102,51 +100,76 @@ template <> struct Cfg<MODE_BF16X6> : CfgBF16 {
 };
 template <> struct Cfg<MODE_TF32X3> : CfgTF32 {
     static constexpr int NCOMP = 2;
-    static constexpr uint32_t SLICE_STAGE = 2 * NCOMP * COMP_TILE;  // 64 KB
     static constexpr int NPROD = 3;
     __host__ __device__ static constexpr int pi(int p) { constexpr int v[3] = {1, 0, 0}; return v[p]; }
     __host__ __device__ static constexpr int pj(int p) { constexpr int v[3] = {0, 1, 0}; return v[p]; }
 };
 template <> struct Cfg<MODE_TF32X1> : CfgTF32 {
     static constexpr int NCOMP = 1;
-    static constexpr uint32_t SLICE_STAGE = 2 * NCOMP * COMP_TILE;  // 32 KB
     static constexpr int NPROD = 1;
     __host__ __device__ static constexpr int pi(int) { return 0; }
     __host__ __device__ static constexpr int pj(int) { return 0; }
 };
 
-// Pipeline depths and output staging, chosen per launch.  Shared memory
-// cannot hold both deep rings and wide staging blocks, so there are two
-// shapes: PIPE_SHORT_K (more FP32 stages, 32-column staging blocks: fastest
-// when a work unit has few k-stages and the output stores come often) and
-// PIPE_LONG_K (three component stages, 16-column blocks: fastest in long
-// k-loops).  TF32x3's larger components leave room for only one shape.
+// Tile width and pipeline shape, chosen per launch.  TN is the pair tile's
+// width (the MMA's N; each CTA holds TN / 2 rows of op(B)^T); TMEM holds
+// 512 / TN accumulators of TN columns, so the MMA can run that many stages
+// ahead of the epilogue.  Shared memory cannot hold both deep rings and wide
+// staging blocks, so there are two shapes:
+//   PIPE_SHORT_K  more FP32 stages and 32-column staging blocks: fastest when
+//                 a work unit has few k-stages and the output stores come
+//                 often;
+//   PIPE_LONG_K   three component stages, 16-column blocks: fastest in long
+//                 k-loops.
+// TF32x3's larger components leave room for only one shape.  A 128-wide
+// tile (four accumulators, so the output stores hide behind the next tile)
+// was measured slower on every workload: the kernel is bound by
+// shared-memory bandwidth (about 90 bytes per clock per SM sustained), and
+// halving the tile width raises the operand bytes per product by half.
 enum Pipe : int { PIPE_SHORT_K = 0, PIPE_LONG_K = 1 };
 template <int MODE, int PIPE> struct PipeCfg;
 template <> struct PipeCfg<MODE_BF16X9, PIPE_SHORT_K> {
-    static constexpr int NF = 3, NS = 2, OUT_COLS = 32;
+    static constexpr int TN = 256, NF = 3, NS = 2, OUT_COLS = 32;
 };
 template <> struct PipeCfg<MODE_BF16X9, PIPE_LONG_K> {
-    static constexpr int NF = 2, NS = 3, OUT_COLS = 16;
+    static constexpr int TN = 256, NF = 2, NS = 3, OUT_COLS = 16;
 };
 template <int PIPE> struct PipeCfg<MODE_BF16X6, PIPE> : PipeCfg<MODE_BF16X9, PIPE> {};
 template <int PIPE> struct PipeCfg<MODE_TF32X3, PIPE> {
-    static constexpr int NF = 2, NS = 2, OUT_COLS = 32;
+    static constexpr int TN = 256, NF = 2, NS = 2, OUT_COLS = 32;
 };
 template <int PIPE> struct PipeCfg<MODE_TF32X1, PIPE> {
-    static constexpr int NF = 3, NS = 3, OUT_COLS = 32;
+    static constexpr int TN = 256, NF = 3, NS = 3, OUT_COLS = 32;
+};
+
+// Everything the kernel derives from (mode, shape).
+template <int MODE, int PIPE> struct KCfg {
+    using C = Cfg<MODE>;
+    using P = PipeCfg<MODE, PIPE>;
+    static constexpr int TN = P::TN;
+    static constexpr int BH = TN / 2;                  // rows of op(B)^T per CTA
+    static constexpr int NACC = TMEM_COLS / TN;        // TMEM accumulators
+    static constexpr int ACC = TN / 2;                 // accumulator registers per epilogue thread
+    static constexpr int NF = P::NF, NS = P::NS, OUT_COLS = P::OUT_COLS;
+    static constexpr uint32_t FP32_B_BYTES = BH * BK * 4;
+    static constexpr uint32_t FP32_STAGE = FP32_TILE_BYTES + FP32_B_BYTES;
+    static constexpr uint32_t COMP_A = C::COMP_TILE;                  // one component of op(A)
+    static constexpr uint32_t COMP_B = BH * C::ROW_BYTES;             // one component of op(B)
+    static constexpr uint32_t SLICE_STAGE = C::NCOMP * (COMP_A + COMP_B);
+    static constexpr uint32_t IDESC = make_idesc(C::KIND, TILE_M, TN);
+    static constexpr uint32_t STAGE_OUT = 32 * OUT_COLS * 4;          // one epilogue warp's staging block
+    static constexpr uint32_t SMEM = 1024 /* alignment slack */ + NF * FP32_STAGE + NS * SLICE_STAGE +
+                                     NUM_EPI_WARPS * STAGE_OUT + 1024 /* barriers and flags */;
+    static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
+    static_assert(NACC * TN == (int)TMEM_COLS && NACC <= 4, "TMEM accumulators");
 };
 
 template <int MODE, int PIPE>
-constexpr uint32_t smem_bytes() {
-    using P = PipeCfg<MODE, PIPE>;
-    return 1024 /* alignment slack */ + P::NF * FP32_STAGE_BYTES + P::NS * Cfg<MODE>::SLICE_STAGE +
-           NUM_EPI_WARPS * (32 * P::OUT_COLS * 4) + 1024 /* barriers and flags */;
-}
+constexpr uint32_t smem_bytes() { return KCfg<MODE, PIPE>::SMEM; }
 
 struct Params {
     CUtensorMap tmA;  // FP32 op(A): K-major box {32, 128} or MN-major box {32, 32}
-    CUtensorMap tmB;  // FP32 op(B): same
+    CUtensorMap tmB;  // FP32 op(B): K-major box {32, TN / 2} or MN-major box {32, 32}
     int M, N, K;
     int a_mn_major, b_mn_major;
     int tiles_m, tiles_n, num_tiles, k_stages;
@@ -157,7 +180,7 @@ struct Params {
     float* c;
     long long ldc;
     const float* bias;   // may be null
-    float* workspace;    // split_k > 1: num_tiles * split_k partial tiles of 256 x 256 (thread-major)
+    float* workspace;    // split_k > 1: num_tiles * split_k partial tiles of 256 x TN (thread-major)
     int* counters;       // split_k > 1: 2 per tile, zero between launches
     unsigned long long wait_budget_ns;
 };
@@ -219,7 +242,9 @@ __device__ __forceinline__ void split_tf32x3_1(float x, uint32_t& hi, uint32_t& 
     lo = tf32_rn_bits(__float_as_uint(__fsub_rn(x, __uint_as_float(hi))));
 }
 
-template <int MODE>
+// Write the components of 8 consecutive k-values of one row; component c of
+// the tile starts at dst + c * CSTRIDE.
+template <int MODE, uint32_t CSTRIDE>
 __device__ __forceinline__ void store_components(uint8_t* dst, uint32_t row, uint32_t g, const float (&x)[8]) {
     using C = Cfg<MODE>;
     if constexpr (!C::TF32) {
@@ -227,8 +252,8 @@ __device__ __forceinline__ void store_components(uint8_t* dst, uint32_t row, uin
         split_bf16x9_8(x, s0, s1, s2);
         const uint32_t o = off_bf16_chunk(row, g);
         *reinterpret_cast<uint4*>(dst + o) = s0;
-        *reinterpret_cast<uint4*>(dst + C::COMP_TILE + o) = s1;
-        *reinterpret_cast<uint4*>(dst + 2 * C::COMP_TILE + o) = s2;
+        *reinterpret_cast<uint4*>(dst + CSTRIDE + o) = s1;
+        *reinterpret_cast<uint4*>(dst + 2 * CSTRIDE + o) = s2;
     } else if constexpr (C::NCOMP == 1) {
         uint32_t h[8];
 #pragma unroll
@@ -243,39 +268,43 @@ __device__ __forceinline__ void store_components(uint8_t* dst, uint32_t row, uin
         const uint32_t o0 = off_f32_chunk(row, 2 * g), o1 = off_f32_chunk(row, 2 * g + 1);
         *reinterpret_cast<uint4*>(dst + o0) = make_uint4(h[0], h[1], h[2], h[3]);
         *reinterpret_cast<uint4*>(dst + o1) = make_uint4(h[4], h[5], h[6], h[7]);
-        *reinterpret_cast<uint4*>(dst + C::COMP_TILE + o0) = make_uint4(l[0], l[1], l[2], l[3]);
-        *reinterpret_cast<uint4*>(dst + C::COMP_TILE + o1) = make_uint4(l[4], l[5], l[6], l[7]);
+        *reinterpret_cast<uint4*>(dst + CSTRIDE + o0) = make_uint4(l[0], l[1], l[2], l[3]);
+        *reinterpret_cast<uint4*>(dst + CSTRIDE + o1) = make_uint4(l[4], l[5], l[6], l[7]);
     }
 }
 
-// Split one operand half-tile (128 rows x 32 k) of a stage.  `src` is the
-// FP32 tile, `dst` the first component tile (components follow at COMP_TILE
-// strides).  `t` is the thread's index among NT split threads (NT a multiple
-// of 32).  Work items are (row, 8-k group) pairs, 512 per tile.
-template <int MODE, int NT>
+// Split one operand tile (ROWS rows x 32 k, ROWS = 128 or 64) of a stage.
+// `src` is the FP32 tile, `dst` the first component tile (components follow
+// at ROWS * ROW_BYTES strides).  `t` is the thread's index among NT split
+// threads (NT a multiple of 32).  Work items are (row, 8-k group) pairs,
+// 4 * ROWS per tile.
+template <int MODE, int NT, int ROWS>
 __device__ __forceinline__ void split_operand(const uint8_t* src, uint8_t* dst, bool mn_major, uint32_t t) {
+    static_assert(ROWS == 128 || ROWS == 64, "tile rows");
+    constexpr uint32_t ITEMS = 4 * ROWS;
+    constexpr uint32_t CSTRIDE = ROWS * Cfg<MODE>::ROW_BYTES;
     if (!mn_major) {
         // lanes cover 8 rows x 4 groups, so both the 16-byte reads and the
         // 16-byte writes of a warp fall on distinct banks
-        for (uint32_t item = t; item < 512u; item += NT) {
+        for (uint32_t item = t; item < ITEMS; item += NT) {
             const uint32_t row = (item >> 5) * 8u + ((item & 31u) >> 2);
             const uint32_t g = item & 3u;
             const float4 lo4 = *reinterpret_cast<const float4*>(src + off_f32_chunk(row, 2 * g));
             const float4 hi4 = *reinterpret_cast<const float4*>(src + off_f32_chunk(row, 2 * g + 1));
             const float x[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
-            store_components<MODE>(dst, row, g, x);
+            store_components<MODE, CSTRIDE>(dst, row, g, x);
         }
     } else {
         // 32 consecutive mn per warp: the column reads of the MN-major tile and
         // the row writes are both conflict-free
-        for (uint32_t item = t; item < 512u; item += NT) {
-            const uint32_t mn = item & 127u;
-            const uint32_t g = item >> 7;
+        for (uint32_t item = t; item < ITEMS; item += NT) {
+            const uint32_t mn = item % ROWS;
+            const uint32_t g = item / ROWS;
             float x[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 x[i] = *reinterpret_cast<const float*>(src + off_f32_mnmajor(mn, 8 * g + i));
-            store_components<MODE>(dst, mn, g, x);
+            store_components<MODE, CSTRIDE>(dst, mn, g, x);
         }
     }
 }
@@ -284,18 +313,19 @@ __device__ __forceinline__ void split_operand(const uint8_t* src, uint8_t* dst, 
 // from zero: the mode's (i, j) component products, smallest first (BF16x9:
 // bands 4, 3, 2, 1, 0; TF32x3: lo*hi, hi*lo, hi*hi), each over the K steps of
 // the stage (two of 16 for BF16, four of 8 for TF32).
-template <int MODE>
+template <int MODE, int PIPE>
 __device__ __forceinline__ void issue_stage_mmas(uint32_t d, uint32_t a_base, uint32_t b_base) {
     using C = Cfg<MODE>;
+    using KC = KCfg<MODE, PIPE>;
     uint32_t acc = 0;
 #pragma unroll
     for (int p = 0; p < C::NPROD; ++p) {
 #pragma unroll
         for (int ks = 0; ks < BK / C::KSTEP; ++ks) {
-            const uint64_t ad = sdesc_kmajor(a_base + C::pi(p) * C::COMP_TILE + ks * 32, C::ROW_BYTES);
-            const uint64_t bd = sdesc_kmajor(b_base + C::pj(p) * C::COMP_TILE + ks * 32, C::ROW_BYTES);
-            if constexpr (C::TF32) mma_tf32_pair(d, ad, bd, C::IDESC, acc);
-            else mma_bf16_pair(d, ad, bd, C::IDESC, acc);
+            const uint64_t ad = sdesc_kmajor(a_base + C::pi(p) * KC::COMP_A + ks * 32, C::ROW_BYTES);
+            const uint64_t bd = sdesc_kmajor(b_base + C::pj(p) * KC::COMP_B + ks * 32, C::ROW_BYTES);
+            if constexpr (C::TF32) mma_tf32_pair(d, ad, bd, KC::IDESC, acc);
+            else mma_bf16_pair(d, ad, bd, KC::IDESC, acc);
             acc = 1;
         }
     }
@@ -317,25 +347,26 @@ template <int MODE, int PIPE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 emu_gemm_kernel(const __grid_constant__ Params p) {
     using C = Cfg<MODE>;
-    using PC = PipeCfg<MODE, PIPE>;
-    constexpr int NF = PC::NF, NS = PC::NS, OUT_COLS = PC::OUT_COLS;
-    constexpr uint32_t STAGE_OUT_BYTES = 32 * OUT_COLS * 4;  // one epilogue warp's 32 x OUT_COLS block
+    using KC = KCfg<MODE, PIPE>;
+    constexpr int NF = KC::NF, NS = KC::NS, OUT_COLS = KC::OUT_COLS;
+    constexpr int TN = KC::TN, BH = KC::BH, NACC = KC::NACC, ACC = KC::ACC;
+    constexpr uint32_t STAGE_OUT_BYTES = KC::STAGE_OUT;  // one epilogue warp's 32 x OUT_COLS block
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // pointer arithmetic on the shared array (not an integer round trip) keeps
     // the shared address space visible to the compiler: shared stores then do
     // not alias global loads, which it can hoist
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* fp32_ring = smem;
-    uint8_t* slice_ring = smem + NF * FP32_STAGE_BYTES;
-    uint8_t* out_stage = slice_ring + NS * C::SLICE_STAGE;  // one block per epilogue warp
+    uint8_t* slice_ring = smem + NF * KC::FP32_STAGE;
+    uint8_t* out_stage = slice_ring + NS * KC::SLICE_STAGE;  // one block per epilogue warp
     uint64_t* bars = reinterpret_cast<uint64_t*>(out_stage + NUM_EPI_WARPS * STAGE_OUT_BYTES);
     uint64_t* fp32_full = bars;
     uint64_t* fp32_empty = fp32_full + NF;
     uint64_t* slice_full = fp32_empty + NF;   // leader: both CTAs' split warps
     uint64_t* slice_empty = slice_full + NS;  // multicast commit
     uint64_t* acc_full = slice_empty + NS;    // multicast commit
-    uint64_t* acc_empty = acc_full + 2;          // leader: both CTAs' epilogue warps
-    uint64_t* drain = acc_empty + 2;
+    uint64_t* acc_empty = acc_full + NACC;    // leader: both CTAs' epilogue warps
+    uint64_t* drain = acc_empty + NACC;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
@@ -344,21 +375,28 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
     const uint32_t rank = cluster_ctarank();
     const uint32_t cid = cluster_id_x(), ncl = num_clusters_x();
 
+    // The next GEMM in the stream may start its own set-up (barriers, TMEM,
+    // the pair barrier) on SMs this grid has left; it touches global memory
+    // only after this grid has completed (griddep_wait).
+    if (threadIdx.x == 0) griddep_launch_dependents();
+
     // The producer's TMA loads for the first FP32 stages need nothing but this
     // CTA's own barriers, so they go out before the pair synchronises and
-    // allocates TMEM (the load latency overlaps the set-up).
+    // allocates TMEM (the load latency overlaps the set-up).  Like every
+    // global access of this kernel they wait for the grids this launch
+    // depends on.
     auto issue_load = [&](int s, int tile, int ks) {
         const int m0 = (tile / p.tiles_n) * TILE_M + HALF * rank;
-        const int n0 = (tile % p.tiles_n) * TILE_N + HALF * rank;
+        const int n0 = (tile % p.tiles_n) * TN + BH * rank;
         uint64_t* full = &fp32_full[s];
-        mbar_arrive_expect_tx(full, FP32_STAGE_BYTES);
-        uint8_t* dA = fp32_ring + s * FP32_STAGE_BYTES;
+        mbar_arrive_expect_tx(full, KC::FP32_STAGE);
+        uint8_t* dA = fp32_ring + s * KC::FP32_STAGE;
         uint8_t* dB = dA + FP32_TILE_BYTES;
         const int k0 = ks * BK;
         if (!p.a_mn_major) tma_load_2d(dA, &p.tmA, full, k0, m0);
-        else for (int j = 0; j < 4; ++j) tma_load_2d(dA + j * 4096, &p.tmA, full, m0 + 32 * j, k0);
+        else for (int j = 0; j < HALF / 32; ++j) tma_load_2d(dA + j * 4096, &p.tmA, full, m0 + 32 * j, k0);
         if (!p.b_mn_major) tma_load_2d(dB, &p.tmB, full, k0, n0);
-        else for (int j = 0; j < 4; ++j) tma_load_2d(dB + j * 4096, &p.tmB, full, n0 + 32 * j, k0);
+        else for (int j = 0; j < BH / 32; ++j) tma_load_2d(dB + j * 4096, &p.tmB, full, n0 + 32 * j, k0);
     };
     int early = 0;  // stages already issued by thread 0 (warp 0 lane 0, the producer)
     if (threadIdx.x == 0) {
@@ -366,10 +404,11 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         tma_prefetch_desc(&p.tmB);
         for (int s = 0; s < NF; ++s) { mbar_init(&fp32_full[s], 1); mbar_init(&fp32_empty[s], 1); }
         for (int s = 0; s < NS; ++s) { mbar_init(&slice_full[s], 2); mbar_init(&slice_empty[s], 1); }
-        for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 2); }
+        for (int b = 0; b < NACC; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 2); }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_mbar_init();
+        griddep_wait();
         for (int u = cid; early < NF && u < p.num_units; u += ncl) {
             const Unit w = unit_of(p, u);
             for (int ks = w.kb; early < NF && ks < w.ke; ++ks, ++early) issue_load(early, w.tile, ks);
@@ -383,6 +422,7 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
     __syncthreads();          // this CTA's barriers and TMEM address visible to all its threads
     cluster_sync_relaxed();   // the peer's barriers initialised before any arrival on them
     tc_fence_after();
+    griddep_wait();           // inputs, C, workspace and counters are the previous grids' to finish
     const uint32_t tmem_base = *tmem_slot;
     const uint64_t budget = p.wait_budget_ns;
 
@@ -429,14 +469,14 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                     if (!mbar_wait(&acc_empty[b], bph ^ 1u, abort_flag, budget, 2)) { ok = false; break; }
                     if (!mbar_wait(&slice_full[s], ph, abort_flag, budget, 2)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_base = slice_base + s * C::SLICE_STAGE;
-                    const uint32_t b_base = a_base + C::NCOMP * C::COMP_TILE;
-                    issue_stage_mmas<MODE>(tmem_base + b * TILE_N, a_base, b_base);
+                    const uint32_t a_base = slice_base + s * KC::SLICE_STAGE;
+                    const uint32_t b_base = a_base + C::NCOMP * KC::COMP_A;
+                    issue_stage_mmas<MODE, PIPE>(tmem_base + b * TN, a_base, b_base);
                     issued = true;
                     mma_commit_pair_multicast(&slice_empty[s], 0x3);
                     mma_commit_pair_multicast(&acc_full[b], 0x3);
                     if (++s == NS) { s = 0; ph ^= 1u; }
-                    if (++b == 2) { b = 0; bph ^= 1u; }
+                    if (++b == NACC) { b = 0; bph ^= 1u; }
                 }
             }
             if (!ok && issued) {
@@ -459,11 +499,11 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
             for (int ks = w.kb; ks < w.ke; ++ks) {
                 if (!mbar_wait_warp(&fp32_full[fs], fph, abort_flag, budget, 3)) { ok = false; break; }
                 if (!mbar_wait_warp(&slice_empty[ss], sph ^ 1u, abort_flag, budget, 3)) { ok = false; break; }
-                const uint8_t* src = fp32_ring + fs * FP32_STAGE_BYTES;
-                uint8_t* dst = slice_ring + ss * C::SLICE_STAGE;
-                split_operand<MODE, NUM_SPLIT_THREADS>(src, dst, p.a_mn_major != 0, t);
-                split_operand<MODE, NUM_SPLIT_THREADS>(src + FP32_TILE_BYTES, dst + C::NCOMP * C::COMP_TILE,
-                                                       p.b_mn_major != 0, t);
+                const uint8_t* src = fp32_ring + fs * KC::FP32_STAGE;
+                uint8_t* dst = slice_ring + ss * KC::SLICE_STAGE;
+                split_operand<MODE, NUM_SPLIT_THREADS, HALF>(src, dst, p.a_mn_major != 0, t);
+                split_operand<MODE, NUM_SPLIT_THREADS, BH>(src + FP32_TILE_BYTES, dst + C::NCOMP * KC::COMP_A,
+                                                           p.b_mn_major != 0, t);
                 // one signal per CTA: the split threads meet, then a single
                 // thread releases the stage (a cluster-scope arrive is costly)
                 fence_proxy_async_smem();
@@ -482,22 +522,22 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         setmaxnreg_inc184();
         const uint32_t e = warp - WARP_EPI0;      // 0..7
         const uint32_t quarter = warp & 3u;       // TMEM lanes this warp may read
-        const uint32_t half = e >> 2;             // which 128 columns of the tile
+        const uint32_t half = e >> 2;             // which TN / 2 columns of the tile
         const uint32_t lane_base = (quarter * 32u) << 16;
         int b = 0;
         uint32_t bph = 0;
         bool ok = true;
         for (int u = cid; ok && u < p.num_units; u += ncl) {
             const Unit w = unit_of(p, u);
-            float acc[128];
+            float acc[ACC];
 #pragma unroll
-            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+            for (int i = 0; i < ACC; ++i) acc[i] = 0.0f;
             for (int ks = w.kb; ks < w.ke; ++ks) {
                 if (!mbar_wait_warp(&acc_full[b], bph, abort_flag, budget, 4)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t col = tmem_base + lane_base + b * TILE_N + half * 128;
+                const uint32_t col = tmem_base + lane_base + b * TN + half * ACC;
 #pragma unroll
-                for (int c = 0; c < 8; c += 2) {
+                for (int c = 0; c < ACC / 16; c += 2) {
                     float v0[16], v1[16];
                     tmem_ld16(col + c * 16, v0);
                     tmem_ld16(col + (c + 1) * 16, v1);
@@ -514,19 +554,19 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                     if (rank == 0) mbar_arrive(&acc_empty[b]);
                     else mbar_arrive_cluster(&acc_empty[b], 0);
                 }
-                if (++b == 2) { b = 0; bph ^= 1u; }
+                if (++b == NACC) { b = 0; bph ^= 1u; }
             }
             if (!ok) break;
             const int row0 = (w.tile / p.tiles_n) * TILE_M + static_cast<int>(HALF * rank + quarter * 32u);
-            const int col0 = (w.tile % p.tiles_n) * TILE_N + static_cast<int>(half * 128u);
+            const int col0 = (w.tile % p.tiles_n) * TN + static_cast<int>(half * ACC);
             if (p.split_k > 1) {
                 // publish this piece's partial (thread-major: each warp store is
                 // 512 contiguous bytes); the last piece to arrive sums all pieces
-                const size_t per_piece = static_cast<size_t>(TILE_M) * TILE_N;
-                const size_t warp_off = (static_cast<size_t>(rank) * NUM_EPI_WARPS + e) * 4096u + lane * 4u;
+                const size_t per_piece = static_cast<size_t>(TILE_M) * TN;
+                const size_t warp_off = (static_cast<size_t>(rank) * NUM_EPI_WARPS + e) * (32u * ACC) + lane * 4u;
                 float* part = p.workspace + (static_cast<size_t>(w.tile) * p.split_k + w.piece) * per_piece + warp_off;
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
+                for (int j = 0; j < ACC / 4; ++j)
                     __stcg(reinterpret_cast<float4*>(part + j * 128),
                            make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
                 __threadfence();
@@ -547,7 +587,7 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                 const float* part0 = p.workspace + static_cast<size_t>(w.tile) * p.split_k * per_piece + warp_off;
                 // (eight float4 loads in flight at a time keeps the registers in budget)
 #pragma unroll
-                for (int jj = 0; jj < 32; jj += 8)
+                for (int jj = 0; jj < ACC / 4; jj += 8)
                 for (int q = 0; q < p.split_k; ++q) {
 #pragma unroll
                     for (int j = jj; j < jj + 8; ++j) {
@@ -563,7 +603,7 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                     }
                 }
             }
-            // 128 / OUT_COLS blocks of 32 rows x OUT_COLS columns: each lane stages
+            // ACC / OUT_COLS blocks of 32 rows x OUT_COLS columns: each lane stages
             // its row's sums in shared memory (rows of OUT_COLS * 4 bytes, 16-byte
             // chunks XOR-swizzled by row); the warp then reads them back as whole
             // row segments, applies C = alpha * acc + beta * C_old + bias and
@@ -578,7 +618,7 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                 return OUT_COLS == 32 ? off_f32_chunk(r, j) : off_bf16_chunk(r, j);
             };
 #pragma unroll
-            for (int c = 0; c < 128 / OUT_COLS; ++c) {
+            for (int c = 0; c < ACC / OUT_COLS; ++c) {
 #pragma unroll
                 for (int j = 0; j < CPR; ++j)
                     *reinterpret_cast<float4*>(stage + chunk_off(lane, j)) =

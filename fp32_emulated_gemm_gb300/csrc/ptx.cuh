@@ -84,6 +84,15 @@ __device__ __forceinline__ uint32_t num_clusters_x() {
     asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
     return r;
 }
+// Programmatic dependent launch.  launch_dependents lets the next kernel in
+// the stream (if it was launched with programmatic serialisation) be
+// scheduled before this grid completes; wait blocks until every grid this
+// one depends on has completed and its memory operations are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // All threads of both CTAs of the pair.
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
