@@ -256,18 +256,22 @@ struct Plan {
 // wider output staging (see PipeCfg).
 constexpr int kLongKMinStages = 16;
 
+// Pairs a plan runs on: for split tiles a multiple of S, so that all pieces
+// of a tile are resident in the same wave (they wait for one another).
+int pairs_for(int split_k, int pairs) { return split_k > 1 ? pairs / split_k * split_k : pairs; }
+
 // Cost of a plan in units of one pipeline stage (measured on GB300): every
-// work unit pays its k-stages plus about 3 stages of output stores (final
-// tile or partial), which the two TMEM accumulators cannot hide; a split
-// tile's last piece also re-reads the other pieces' partials (about 1.5
-// stages each) and stores the final tile.  Units run in waves over the
-// resident CTA pairs.
+// work unit pays its k-stages plus about 3 stages of output stores, which the
+// two TMEM accumulators cannot hide; split tiles add the reduce-scatter
+// (publishing (S-1)/S of a partial tile and reading the owned parts back),
+// about 1.5 stages.  Units run in waves over the resident CTA pairs.
 double plan_cost(long long tiles, int k_stages, int S, int pairs) {
     const long long units = tiles * S;
-    const long long waves = (units + pairs - 1) / pairs;
+    const long long used = pairs_for(S, pairs);
+    const long long waves = (units + used - 1) / used;
     const long long per = (k_stages + S - 1) / S;
     double cost = (double)waves * (double)(per + 3);
-    if (S > 1) cost += 1.5 * (S - 1) + 3.0;
+    if (S > 1) cost += 1.5;
     return cost;
 }
 
@@ -287,10 +291,14 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int pairs) {
     plan.k_stages = (int)((K + BK - 1) / BK);
     const int force_split = env_int("EMU_SPLIT_K", 0);
     if (force_split >= 1) {
-        plan.split_k = force_split < plan.k_stages ? force_split : plan.k_stages;
+        int S = force_split < plan.k_stages ? force_split : plan.k_stages;
+        S = S < pairs ? S : pairs;
+        plan.split_k = S < 32 ? S : 32;
     } else {
         double best_cost = -1.0;
-        for (int S = 1; S <= 64 && S <= plan.k_stages; ++S) {
+        // a split tile's S pieces all wait for one another: at most one per
+        // resident pair, and at most one per 32-column chunk of a CTA's half
+        for (int S = 1; S <= 32 && S <= plan.k_stages && S <= pairs; ++S) {
             if (S > 1 && plan.k_stages / S < 2) break;
             const double cost = plan_cost(plan.num_tiles, plan.k_stages, S, pairs);
             if (best_cost < 0 || cost < best_cost - 1e-9) { best_cost = cost; plan.split_k = S; }
@@ -415,12 +423,13 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
         cudaGetDevice(&devid);
         Workspace* w = nullptr;
         const size_t floats = (size_t)p.num_tiles * p.split_k * TILE_M * plan.tn;
-        st = workspace_for(devid, stream, floats, (size_t)p.num_tiles * 2, &w);
+        st = workspace_for(devid, stream, floats, (size_t)p.num_tiles * 4, &w);
         if (st != EMU_STATUS_SUCCESS) return st;
         p.workspace = w->partials;
         p.counters = w->counters;
     }
-    const int clusters = p.num_units < pairs ? p.num_units : pairs;
+    const int used = pairs_for(p.split_k, pairs);
+    const int clusters = p.num_units < used ? p.num_units : used;
     if (log_enabled())
         std::fprintf(stderr, "[emu] %s M=%lld N=%lld K=%lld a_mn=%d b_mn=%d pipe=%d tile=256x%d tiles=%dx%d "
                              "k_stages=%d split_k=%d units=%d pairs=%d (max %d)\n",
@@ -693,7 +702,7 @@ emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, 
         // partial tiles first, then one counter per CTA half-tile
         const size_t partial_bytes = (size_t)p.num_tiles * p.split_k * TILE_M * plan.tn * sizeof(float);
         const size_t counter_off = (partial_bytes + 255) & ~size_t(255);
-        const size_t counter_bytes = (size_t)p.num_tiles * 2 * sizeof(int);
+        const size_t counter_bytes = (size_t)p.num_tiles * 4 * sizeof(int);
         if (counter_off + counter_bytes > kNoAllocScratchBytes) return EMU_STATUS_NOT_SUPPORTED;
         p.workspace = reinterpret_cast<float*>(scratch);
         p.counters = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(scratch) + counter_off);
@@ -703,7 +712,8 @@ emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, 
             return EMU_STATUS_LAUNCH_FAILED;
         }
     }
-    const int clusters = p.num_units < pairs ? p.num_units : pairs;
+    const int used = pairs_for(p.split_k, pairs);
+    const int clusters = p.num_units < used ? p.num_units : used;
     return launch_gemm(mode, plan.pipe, p, clusters, stream) == cudaSuccess ? EMU_STATUS_SUCCESS
                                                                              : EMU_STATUS_LAUNCH_FAILED;
 }

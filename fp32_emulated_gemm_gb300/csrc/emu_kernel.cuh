@@ -33,10 +33,11 @@
 // as the blog reports for BF16x9 ("Limitations and decision criteria").
 //
 // Split-K: when there are too few tiles to fill the GPU, a tile's k-range is
-// cut into S pieces processed by different pairs.  Each piece writes its
-// partial tile to a workspace; the last piece to finish (per-tile counter)
-// adds the S partials in the fixed order 0..S-1 -- the result does not depend
-// on which piece finishes last -- and applies the epilogue.
+// cut into S pieces processed by different pairs at the same time.  The
+// pieces reduce-scatter through a workspace: each publishes the parts of its
+// partial tile that the others own, and sums and stores its own part, adding
+// the S partials in the fixed order 0..S-1 -- the result does not depend on
+// timing.
 #pragma once
 
 #include <cstdint>
@@ -181,7 +182,7 @@ struct Params {
     long long ldc;
     const float* bias;   // may be null
     float* workspace;    // split_k > 1: num_tiles * split_k partial tiles of 256 x TN (thread-major)
-    int* counters;       // split_k > 1: 2 per tile, zero between launches
+    int* counters;       // split_k > 1: 4 per tile (published, finished per CTA half), zero between launches
     unsigned long long wait_budget_ns;
 };
 
@@ -559,47 +560,66 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
             if (!ok) break;
             const int row0 = (w.tile / p.tiles_n) * TILE_M + static_cast<int>(HALF * rank + quarter * 32u);
             const int col0 = (w.tile % p.tiles_n) * TN + static_cast<int>(half * ACC);
-            if (p.split_k > 1) {
-                // publish this piece's partial (thread-major: each warp store is
-                // 512 contiguous bytes); the last piece to arrive sums all pieces
+            // Split tiles: a reduce-scatter over the tile's S pieces, which all
+            // run at the same time (the pairs in use are a multiple of S, so a
+            // tile's pieces fall in one wave).  Chunk q = 4e + c (32 columns of
+            // warp e's block) of this CTA's half-tile belongs to piece q mod S.
+            // Each piece publishes the chunks that other pieces own, waits until
+            // all S pieces have published, and sums the chunks it owns -- its own
+            // partial, then the other pieces' in increasing piece order, a fixed
+            // order for every chunk -- and stores only those: the result does not
+            // depend on timing.
+            const int S = p.split_k;
+            auto owns = [&](int c) { return S == 1 || static_cast<int>(4 * e + c) % S == w.piece; };
+            if (S > 1) {
                 const size_t per_piece = static_cast<size_t>(TILE_M) * TN;
                 const size_t warp_off = (static_cast<size_t>(rank) * NUM_EPI_WARPS + e) * (32u * ACC) + lane * 4u;
-                float* part = p.workspace + (static_cast<size_t>(w.tile) * p.split_k + w.piece) * per_piece + warp_off;
+                float* tile_ws = p.workspace + static_cast<size_t>(w.tile) * S * per_piece + warp_off;
+                float* part = tile_ws + static_cast<size_t>(w.piece) * per_piece;
+                // (thread-major: float4 j of every lane of a warp is 512
+                // contiguous bytes; chunk c is j in [8c, 8c + 8))
 #pragma unroll
                 for (int j = 0; j < ACC / 4; ++j)
-                    __stcg(reinterpret_cast<float4*>(part + j * 128),
-                           make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
+                    if (!owns(j / 8))
+                        __stcg(reinterpret_cast<float4*>(part + j * 128),
+                               make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
                 __threadfence();
                 named_bar_sync(EPI_BARRIER, NUM_EPI_WARPS * 32);
+                int* ctr = p.counters + (static_cast<size_t>(w.tile) * 2 + rank) * 2;  // published, finished
                 if (e == 0 && lane == 0) {
-                    int* ctr = p.counters + w.tile * 2 + rank;
-                    const int prev = atomicAdd(ctr, 1);
-                    const int last = prev == p.split_k - 1;
-                    if (last) atomicExch(ctr, 0);  // ready for the next launch
-                    *last_flag = last;
+                    atomicAdd(&ctr[0], 1);
+                    *last_flag = wait_count_geq(&ctr[0], S, abort_flag, budget, 6) ? 1 : 0;
                 }
                 named_bar_sync(EPI_BARRIER, NUM_EPI_WARPS * 32);
-                const int is_last = *last_flag;
+                const int published = *last_flag;
                 named_bar_sync(EPI_BARRIER, NUM_EPI_WARPS * 32);  // flag read before the next unit rewrites it
-                if (!is_last) continue;
+                if (!published) { ok = false; break; }
                 __threadfence();
-                // fixed order 0, 1, ..., S-1, whichever piece arrived last
-                const float* part0 = p.workspace + static_cast<size_t>(w.tile) * p.split_k * per_piece + warp_off;
-                // (eight float4 loads in flight at a time keeps the registers in budget)
+                // the owner's own partial first, then the other pieces in
+                // increasing order, added in place (a fixed order per chunk)
 #pragma unroll
-                for (int jj = 0; jj < ACC / 4; jj += 8)
-                for (int q = 0; q < p.split_k; ++q) {
+                for (int c = 0; c < ACC / 32; ++c) {
+                    if (!owns(c)) continue;
+                    for (int q = 0; q < S; ++q) {
+                        if (q == w.piece) continue;
+                        const float* src = tile_ws + static_cast<size_t>(q) * per_piece + c * 1024;
+                        float4 x[8];
 #pragma unroll
-                    for (int j = jj; j < jj + 8; ++j) {
-                        const float4 v = __ldcg(reinterpret_cast<const float4*>(part0 + q * per_piece + j * 128));
-                        if (q == 0) {
-                            acc[4 * j] = v.x; acc[4 * j + 1] = v.y; acc[4 * j + 2] = v.z; acc[4 * j + 3] = v.w;
-                        } else {
-                            acc[4 * j] = __fadd_rn(acc[4 * j], v.x);
-                            acc[4 * j + 1] = __fadd_rn(acc[4 * j + 1], v.y);
-                            acc[4 * j + 2] = __fadd_rn(acc[4 * j + 2], v.z);
-                            acc[4 * j + 3] = __fadd_rn(acc[4 * j + 3], v.w);
+                        for (int j = 0; j < 8; ++j) x[j] = __ldcg(reinterpret_cast<const float4*>(src + j * 128));
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            acc[32 * c + 4 * j] = __fadd_rn(acc[32 * c + 4 * j], x[j].x);
+                            acc[32 * c + 4 * j + 1] = __fadd_rn(acc[32 * c + 4 * j + 1], x[j].y);
+                            acc[32 * c + 4 * j + 2] = __fadd_rn(acc[32 * c + 4 * j + 2], x[j].z);
+                            acc[32 * c + 4 * j + 3] = __fadd_rn(acc[32 * c + 4 * j + 3], x[j].w);
                         }
+                    }
+                }
+                named_bar_sync(EPI_BARRIER, NUM_EPI_WARPS * 32);  // this CTA's reads of the partials are done
+                if (e == 0 && lane == 0) {
+                    if (atomicAdd(&ctr[1], 1) == S - 1) {  // the tile's last reader: ready for the next launch
+                        atomicExch(&ctr[0], 0);
+                        atomicExch(&ctr[1], 0);
                     }
                 }
             }
@@ -619,6 +639,7 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
             };
 #pragma unroll
             for (int c = 0; c < ACC / OUT_COLS; ++c) {
+                if (!owns(c * OUT_COLS / 32)) continue;  // another piece of a split tile stores it
 #pragma unroll
                 for (int j = 0; j < CPR; ++j)
                     *reinterpret_cast<float4*>(stage + chunk_off(lane, j)) =

@@ -124,6 +124,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// Single-thread wait until the global counter reaches `target` (acquire at
+// GPU scope, so that the writes the other CTAs released before incrementing
+// it are visible), bounded like the barrier waits.
+__device__ __forceinline__ bool wait_count_geq(const int* ctr, int target, volatile int* abort,
+                                               uint64_t budget_ns, unsigned role) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= target) return true;
+        if ((i & 7u) == 7u) {
+            if (*abort) return false;
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0) {
+                t0 = now;
+            } else if (now - t0 > budget_ns) {
+                atomicOr(&g_error_flag, ERR_TIMEOUT | (role << 8));
+                *abort = 1;
+                return false;
+            }
+        }
+        __nanosleep(64);
+    }
+}
+
 // Warp-collective form: every lane polls, and the warp stops together, so
 // that the .sync.aligned instructions that follow see a converged warp.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,

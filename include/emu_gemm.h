@@ -177,7 +177,7 @@ emu_status_t emu_split_dump(emu_mode_t mode, int64_t R, int64_t Kc, const float 
  * array is reserved on every GPU that loads the library and kept until the
  * process exits.
  *   - Size limit: a plan that splits K into S pieces needs
- *     tiles * S * 256 KiB (+ 8 bytes per tile, tiles = ceil(M/256) *
+ *     tiles * S * 256 KiB (+ 16 bytes per tile, tiles = ceil(M/256) *
  *     ceil(N/256)); if that exceeds 64 MiB the call returns
  *     EMU_STATUS_NOT_SUPPORTED and enqueues nothing.  Plans without a split
  *     use no scratch and are never rejected for size.

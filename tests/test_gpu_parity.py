@@ -239,3 +239,30 @@ def test_comparator_modes(mode):
     assert emu.emu_stream_check() == 0
     _gpu.compare(mode, Y.cpu().numpy(), oracle.Problem(X, Wt, transB=True, bias=b), rows)
     _gpu.compare(mode, dX.cpu().numpy(), oracle.Problem(dY, Wt), rows)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_split_k_plans_match_oracle_and_repeat_bitwise(mode, monkeypatch):
+    """A long-k, few-tile GEMM under forced split-K plans (the pieces of a
+    tile reduce-scatter their partials through the workspace): every plan
+    meets the tolerances, and each plan gives the same bits on every run
+    (the sum order is fixed by the plan, not by which piece finishes first)."""
+    import torch
+    import fp32_emulated_gemm_gb300 as emu
+    rng = np.random.default_rng(11)
+    M, N, K = 300, 260, 3000          # 2 x 2 tiles, ragged edges, 94 k-stages
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    B = (rng.standard_normal((K, N)) / np.sqrt(K)).astype(np.float32)
+    Ad, Bd = _gpu.to_dev_padded(A, float("nan")), _gpu.to_dev_padded(B, float("nan"))
+    noise = torch.empty(1 << 22, device=_gpu.device())
+    for S in ("1", "2", "3", "7"):
+        monkeypatch.setenv("EMU_SPLIT_K", S)
+        runs = []
+        for rep in range(3):
+            noise.uniform_()  # other work on the GPU between runs
+            C = emu.sgemm(Ad, Bd, mode=mode)
+            assert emu.emu_stream_check() == 0
+            runs.append(C.cpu().numpy())
+        for r in runs[1:]:
+            assert np.array_equal(r.view(np.uint32), runs[0].view(np.uint32)), f"split {S} not repeatable"
+        _gpu.compare(mode, runs[0], oracle.Problem(A, B))
