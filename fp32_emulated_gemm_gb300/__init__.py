@@ -21,7 +21,7 @@ __all__ = [
     "EMU_MODE_BF16X9", "EMU_MODE_TF32X3", "EMU_MODE_TF32X1", "EMU_MODE_BF16X6", "EMU_OP_N", "EMU_OP_T",
     "EmuError",
     "emu_sgemm", "emu_linear_fwd", "emu_linear_bwd_input", "emu_linear_bwd_weight", "emu_status_string",
-    "emu_stream_check", "emu_split_dump", "emu_version",
+    "emu_stream_check", "emu_split_dump", "emu_plan_query", "emu_version",
     "sgemm", "linear_fwd", "linear_bwd_input", "linear_bwd_weight", "EmuLinearFunction", "EmuLinear",
     "library_path", "load",
 ]
@@ -76,6 +76,8 @@ def load():
         L.emu_status_string.restype = ctypes.c_char_p
         L.emu_stream_check.argtypes = [P]
         L.emu_split_dump.argtypes = [i32, i64, i64, P, i64, i32, P, P]
+        L.emu_plan_query.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64), i32]
+        L.emu_plan_query.restype = i32
         L.emu_version.argtypes = []
         for name in ("emu_sgemm", "emu_linear_fwd", "emu_linear_bwd_input", "emu_linear_bwd_weight",
                      "emu_stream_check",
@@ -134,6 +136,17 @@ def emu_stream_check(stream=None) -> int:
 def emu_split_dump(mode, R, Kc, X, ldx, mn_major, out, stream=None):
     _check(load().emu_split_dump(int(mode), int(R), int(Kc), _ptr(X), int(ldx), int(mn_major), _ptr(out),
                                  ctypes.c_void_p(_stream(stream))), "emu_split_dump")
+
+
+PLAN_FIELDS = ("pipe", "tile_n", "tiles_m", "tiles_n", "k_stages", "tiles_a", "split_a", "split_b",
+               "units", "pairs", "slots")
+
+
+def emu_plan_query(M, N, K, pairs) -> dict:
+    """The launch plan emu_sgemm would use (host only; see the header)."""
+    out = (ctypes.c_int64 * len(PLAN_FIELDS))()
+    _check(load().emu_plan_query(int(M), int(N), int(K), int(pairs), out, len(PLAN_FIELDS)), "emu_plan_query")
+    return dict(zip(PLAN_FIELDS, (int(v) for v in out)))
 
 
 def emu_version() -> int:

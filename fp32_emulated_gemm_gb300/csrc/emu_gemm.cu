@@ -245,43 +245,42 @@ emu_status_t workspace_for(int dev, cudaStream_t stream, size_t floats, size_t c
     return EMU_STATUS_SUCCESS;
 }
 
-// The launch plan: pipeline shape, tiles and pieces per tile.
+// The launch plan: pipeline shape, tiles, and how tiles become work units.
 struct Plan {
     int pipe;       // PIPE_SHORT_K or PIPE_LONG_K
     int tn;         // pair tile width
-    int tiles_m, tiles_n, num_tiles, k_stages, split_k;
+    int tiles_m, tiles_n, num_tiles, k_stages;
+    int tiles_a, split_a, split_b;  // see Params
+    int num_units;
+    int clusters;   // CTA pairs launched
+    long long slots;  // workspace partial tiles (0: no split tile)
 };
 
 // Long k-loops per work unit favour three component stages; short ones the
 // wider output staging (see PipeCfg).
 constexpr int kLongKMinStages = 16;
 
-// Pairs a plan runs on: for split tiles a multiple of S, so that all pieces
-// of a tile are resident in the same wave (they wait for one another).
-int pairs_for(int split_k, int pairs) { return split_k > 1 ? pairs / split_k * split_k : pairs; }
-
-// Cost of a plan in units of one pipeline stage (measured on GB300): every
-// work unit pays its k-stages plus about 3 stages of output stores, which the
-// two TMEM accumulators cannot hide; split tiles add the reduce-scatter
-// (publishing (S-1)/S of a partial tile and reading the owned parts back),
-// about 1.5 stages.  Units run in waves over the resident CTA pairs.
-double plan_cost(long long tiles, int k_stages, int S, int pairs) {
-    const long long units = tiles * S;
-    const long long used = pairs_for(S, pairs);
-    const long long waves = (units + used - 1) / used;
-    const long long per = (k_stages + S - 1) / S;
-    double cost = (double)waves * (double)(per + 3);
-    if (S > 1) cost += 1.5;
-    return cost;
-}
+// Costs in units of one pipeline stage (measured on GB300): every work unit
+// pays its k-stages plus about 3 stages of output stores, which the two TMEM
+// accumulators cannot hide; split tiles add the reduce-scatter (publishing
+// (S-1)/S of a partial tile and reading the owned parts back), about 1.5
+// stages.  Units run in waves over the resident CTA pairs.
+constexpr double kStoreStages = 3.0, kReduceStages = 1.5;
 
 int env_int(const char* name, int dflt) {
     const char* v = std::getenv(name);
     return v ? std::atoi(v) : dflt;
 }
 
-// EMU_SPLIT_K and EMU_PIPE (0 short-k, 1 long-k) override the choice, for
-// diagnostics and tuning.
+// Candidate plans (a split tile's S pieces wait for one another, so they
+// must run in the same wave of units: S is at most the number of pairs, and
+// at most 32, the 32-column chunks of a CTA's half-tile):
+//   uniform: every tile in S pieces; with more than one wave the pairs in
+//     use are a multiple of S, so that waves hold whole tiles;
+//   hybrid: W full waves of whole tiles on all pairs, then the remaining
+//     tiles (fewer than the pairs) in S pieces, one more wave at most.
+// EMU_SPLIT_K (uniform S) and EMU_PIPE (0 short-k, 1 long-k) override the
+// choice, for diagnostics and tuning.
 Plan make_plan(int64_t M, int64_t N, int64_t K, int pairs) {
     Plan plan{};
     plan.tn = 256;
@@ -289,22 +288,49 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int pairs) {
     plan.tiles_n = (int)((N + plan.tn - 1) / plan.tn);
     plan.num_tiles = plan.tiles_m * plan.tiles_n;
     plan.k_stages = (int)((K + BK - 1) / BK);
+    const long long T = plan.num_tiles;
+    const int KS = plan.k_stages;
+    auto set_uniform = [&](int S) {
+        plan.tiles_a = (int)T; plan.split_a = S; plan.split_b = 1;
+        const long long units = T * S;
+        const long long used = units <= pairs || S == 1 ? pairs : pairs / S * S;
+        plan.clusters = (int)(units < used ? units : used);
+    };
+    auto cost_uniform = [&](int S) {
+        const long long units = T * S;
+        const long long used = units <= pairs || S == 1 ? pairs : pairs / S * S;
+        const long long waves = (units + used - 1) / used;
+        return (double)waves * ((KS + S - 1) / S + kStoreStages) + (S > 1 ? kReduceStages : 0.0);
+    };
     const int force_split = env_int("EMU_SPLIT_K", 0);
+    const int s_max = KS < 32 ? KS : 32;
     if (force_split >= 1) {
-        int S = force_split < plan.k_stages ? force_split : plan.k_stages;
-        S = S < pairs ? S : pairs;
-        plan.split_k = S < 32 ? S : 32;
+        int S = force_split < s_max ? force_split : s_max;
+        set_uniform(S < pairs ? S : pairs);
     } else {
-        double best_cost = -1.0;
-        // a split tile's S pieces all wait for one another: at most one per
-        // resident pair, and at most one per 32-column chunk of a CTA's half
-        for (int S = 1; S <= 32 && S <= plan.k_stages && S <= pairs; ++S) {
-            if (S > 1 && plan.k_stages / S < 2) break;
-            const double cost = plan_cost(plan.num_tiles, plan.k_stages, S, pairs);
-            if (best_cost < 0 || cost < best_cost - 1e-9) { best_cost = cost; plan.split_k = S; }
+        double best = -1.0;
+        for (int S = 1; S <= s_max && S <= pairs; ++S) {
+            if (S > 1 && KS / S < 2) break;
+            const double c = cost_uniform(S);
+            if (best < 0 || c < best - 1e-9) { best = c; set_uniform(S); }
+        }
+        const long long W = T / pairs, tail = T - W * pairs;
+        if (W >= 1 && tail >= 1) {
+            for (int S = 2; S <= s_max && tail * S <= pairs; ++S) {
+                if (KS / S < 2) break;
+                const double c = (double)W * (KS + kStoreStages) + ((KS + S - 1) / S + kStoreStages) + kReduceStages;
+                if (c < best - 1e-9) {
+                    best = c;
+                    plan.tiles_a = (int)(W * pairs); plan.split_a = 1; plan.split_b = S;
+                    plan.clusters = pairs;
+                }
+            }
         }
     }
-    const int per_unit = (plan.k_stages + plan.split_k - 1) / plan.split_k;
+    plan.num_units = plan.tiles_a * plan.split_a + (plan.num_tiles - plan.tiles_a) * plan.split_b;
+    plan.slots = (plan.split_a > 1 ? (long long)plan.tiles_a * plan.split_a : 0) +
+                 (plan.split_b > 1 ? (long long)(plan.num_tiles - plan.tiles_a) * plan.split_b : 0);
+    const int per_unit = (KS + plan.split_a - 1) / plan.split_a;
     const int force_pipe = env_int("EMU_PIPE", -1);
     plan.pipe = force_pipe == PIPE_SHORT_K || force_pipe == PIPE_LONG_K ? force_pipe
               : per_unit >= kLongKMinStages ? PIPE_LONG_K : PIPE_SHORT_K;
@@ -412,29 +438,29 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
     p.tiles_n = plan.tiles_n;
     p.num_tiles = plan.num_tiles;
     p.k_stages = plan.k_stages;
-    p.split_k = plan.split_k;
-    p.num_units = p.num_tiles * p.split_k;
+    p.tiles_a = plan.tiles_a; p.split_a = plan.split_a; p.split_b = plan.split_b;
+    p.num_units = plan.num_units;
     p.alpha = alpha; p.beta = beta;
     p.c_old = C; p.c = C; p.ldc = ldc;
     p.bias = bias;
     p.wait_budget_ns = wait_budget_ns();
-    if (p.split_k > 1) {
+    if (plan.slots > 0) {
         int devid = 0;
         cudaGetDevice(&devid);
         Workspace* w = nullptr;
-        const size_t floats = (size_t)p.num_tiles * p.split_k * TILE_M * plan.tn;
+        const size_t floats = (size_t)plan.slots * TILE_M * plan.tn;
         st = workspace_for(devid, stream, floats, (size_t)p.num_tiles * 4, &w);
         if (st != EMU_STATUS_SUCCESS) return st;
         p.workspace = w->partials;
         p.counters = w->counters;
     }
-    const int used = pairs_for(p.split_k, pairs);
-    const int clusters = p.num_units < used ? p.num_units : used;
+    const int clusters = plan.clusters;
     if (log_enabled())
         std::fprintf(stderr, "[emu] %s M=%lld N=%lld K=%lld a_mn=%d b_mn=%d pipe=%d tile=256x%d tiles=%dx%d "
-                             "k_stages=%d split_k=%d units=%d pairs=%d (max %d)\n",
+                             "k_stages=%d units=%d (%d tiles x %d, then x %d) pairs=%d (max %d)\n",
                      mode_name(mode), (long long)M, (long long)N, (long long)K, (int)a_mn, (int)b_mn, plan.pipe,
-                     plan.tn, p.tiles_m, p.tiles_n, p.k_stages, p.split_k, p.num_units, clusters, pairs);
+                     plan.tn, p.tiles_m, p.tiles_n, p.k_stages, p.num_units, p.tiles_a, p.split_a, p.split_b,
+                     clusters, pairs);
     return launch_gemm(mode, plan.pipe, p, clusters, stream) == cudaSuccess ? EMU_STATUS_SUCCESS
                                                                              : EMU_STATUS_LAUNCH_FAILED;
 }
@@ -603,6 +629,16 @@ emu_status_t emu_selftest_wait_timeout(uint64_t budget_ns, emu_stream_t stream) 
     return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
 }
 
+emu_status_t emu_plan_query(int64_t M, int64_t N, int64_t K, int pairs, int64_t* out, int n) {
+    if (M <= 0 || N <= 0 || K <= 0 || pairs < 1 || !out || n < EMU_PLAN_FIELDS) return EMU_STATUS_INVALID_VALUE;
+    if (M > INT32_MAX - 256 || N > INT32_MAX - 256 || K > INT32_MAX - 256) return EMU_STATUS_NOT_SUPPORTED;
+    const Plan p = make_plan(M, N, K, pairs);
+    const int64_t v[EMU_PLAN_FIELDS] = {p.pipe, p.tn, p.tiles_m, p.tiles_n, p.k_stages, p.tiles_a,
+                                        p.split_a, p.split_b, p.num_units, p.clusters, p.slots};
+    for (int i = 0; i < EMU_PLAN_FIELDS; ++i) out[i] = v[i];
+    return EMU_STATUS_SUCCESS;
+}
+
 int emu_version(void) { return 100; }
 
 }  // extern "C"
@@ -692,15 +728,15 @@ emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, 
     p.tiles_n = plan.tiles_n;
     p.num_tiles = plan.num_tiles;
     p.k_stages = plan.k_stages;
-    p.split_k = plan.split_k;
-    p.num_units = p.num_tiles * p.split_k;
+    p.tiles_a = plan.tiles_a; p.split_a = plan.split_a; p.split_b = plan.split_b;
+    p.num_units = plan.num_units;
     p.alpha = alpha; p.beta = beta;
     p.c_old = C; p.c = C; p.ldc = ldc;
     p.bias = nullptr;
     p.wait_budget_ns = wait_budget_ns();
-    if (p.split_k > 1) {
-        // partial tiles first, then one counter per CTA half-tile
-        const size_t partial_bytes = (size_t)p.num_tiles * p.split_k * TILE_M * plan.tn * sizeof(float);
+    if (plan.slots > 0) {
+        // partial tiles first, then the counters
+        const size_t partial_bytes = (size_t)plan.slots * TILE_M * plan.tn * sizeof(float);
         const size_t counter_off = (partial_bytes + 255) & ~size_t(255);
         const size_t counter_bytes = (size_t)p.num_tiles * 4 * sizeof(int);
         if (counter_off + counter_bytes > kNoAllocScratchBytes) return EMU_STATUS_NOT_SUPPORTED;
@@ -712,8 +748,7 @@ emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, 
             return EMU_STATUS_LAUNCH_FAILED;
         }
     }
-    const int used = pairs_for(p.split_k, pairs);
-    const int clusters = p.num_units < used ? p.num_units : used;
+    const int clusters = plan.clusters;
     return launch_gemm(mode, plan.pipe, p, clusters, stream) == cudaSuccess ? EMU_STATUS_SUCCESS
                                                                              : EMU_STATUS_LAUNCH_FAILED;
 }

@@ -174,15 +174,19 @@ struct Params {
     int M, N, K;
     int a_mn_major, b_mn_major;
     int tiles_m, tiles_n, num_tiles, k_stages;
-    int split_k;      // pieces per tile (1 = no split)
-    int num_units;    // num_tiles * split_k
+    // Work units: the first tiles_a tiles in split_a pieces each, then the
+    // remaining tiles in split_b pieces each (1 = the whole tile).  Units are
+    // numbered tile by tile, pieces in k order; CTA pair c takes units c,
+    // c + pairs, c + 2 pairs, ...
+    int tiles_a, split_a, split_b;
+    int num_units;
     float alpha, beta;
     const float* c_old;  // read only when beta != 0
     float* c;
     long long ldc;
     const float* bias;   // may be null
-    float* workspace;    // split_k > 1: num_tiles * split_k partial tiles of 256 x TN (thread-major)
-    int* counters;       // split_k > 1: 4 per tile (published, finished per CTA half), zero between launches
+    float* workspace;    // split tiles: S partial tiles of 256 x TN each (thread-major)
+    int* counters;       // split tiles: 4 per tile (published, finished per CTA half), zero between launches
     unsigned long long wait_budget_ns;
 };
 
@@ -333,14 +337,28 @@ __device__ __forceinline__ void issue_stage_mmas(uint32_t d, uint32_t a_base, ui
 }
 
 struct Unit {
-    int tile, piece, kb, ke;
+    int tile, piece, pieces, kb, ke;
+    long long slot;  // first workspace partial tile of a split tile
 };
 __device__ __forceinline__ Unit unit_of(const Params& p, int u) {
     Unit w;
-    w.tile = u / p.split_k;
-    w.piece = u - w.tile * p.split_k;
-    w.kb = static_cast<int>((static_cast<long long>(w.piece) * p.k_stages) / p.split_k);
-    w.ke = static_cast<int>((static_cast<long long>(w.piece + 1) * p.k_stages) / p.split_k);
+    const int units_a = p.tiles_a * p.split_a;
+    const long long slots_a = p.split_a > 1 ? static_cast<long long>(units_a) : 0;
+    if (u < units_a) {
+        w.pieces = p.split_a;
+        w.tile = u / p.split_a;
+        w.piece = u - w.tile * p.split_a;
+        w.slot = static_cast<long long>(w.tile) * p.split_a;
+    } else {
+        const int v = u - units_a;
+        const int t = v / p.split_b;
+        w.pieces = p.split_b;
+        w.tile = p.tiles_a + t;
+        w.piece = v - t * p.split_b;
+        w.slot = slots_a + static_cast<long long>(t) * p.split_b;
+    }
+    w.kb = static_cast<int>((static_cast<long long>(w.piece) * p.k_stages) / w.pieces);
+    w.ke = static_cast<int>((static_cast<long long>(w.piece + 1) * p.k_stages) / w.pieces);
     return w;
 }
 
@@ -561,20 +579,20 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
             const int row0 = (w.tile / p.tiles_n) * TILE_M + static_cast<int>(HALF * rank + quarter * 32u);
             const int col0 = (w.tile % p.tiles_n) * TN + static_cast<int>(half * ACC);
             // Split tiles: a reduce-scatter over the tile's S pieces, which all
-            // run at the same time (the pairs in use are a multiple of S, so a
-            // tile's pieces fall in one wave).  Chunk q = 4e + c (32 columns of
+            // run at the same time (the plan keeps a tile's pieces in one wave
+            // of units).  Chunk q = 4e + c (32 columns of
             // warp e's block) of this CTA's half-tile belongs to piece q mod S.
             // Each piece publishes the chunks that other pieces own, waits until
             // all S pieces have published, and sums the chunks it owns -- its own
             // partial, then the other pieces' in increasing piece order, a fixed
             // order for every chunk -- and stores only those: the result does not
             // depend on timing.
-            const int S = p.split_k;
+            const int S = w.pieces;
             auto owns = [&](int c) { return S == 1 || static_cast<int>(4 * e + c) % S == w.piece; };
             if (S > 1) {
                 const size_t per_piece = static_cast<size_t>(TILE_M) * TN;
                 const size_t warp_off = (static_cast<size_t>(rank) * NUM_EPI_WARPS + e) * (32u * ACC) + lane * 4u;
-                float* tile_ws = p.workspace + static_cast<size_t>(w.tile) * S * per_piece + warp_off;
+                float* tile_ws = p.workspace + static_cast<size_t>(w.slot) * per_piece + warp_off;
                 float* part = tile_ws + static_cast<size_t>(w.piece) * per_piece;
                 // (thread-major: float4 j of every lane of a warp is 512
                 // contiguous bytes; chunk c is j in [8c, 8c + 8))

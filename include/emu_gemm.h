@@ -176,8 +176,8 @@ emu_status_t emu_split_dump(emu_mode_t mode, int64_t R, int64_t Kc, const float 
  * lives in a fixed 64 MiB device array inside the library instead.  The
  * array is reserved on every GPU that loads the library and kept until the
  * process exits.
- *   - Size limit: a plan that splits K into S pieces needs
- *     tiles * S * 256 KiB (+ 16 bytes per tile, tiles = ceil(M/256) *
+ *   - Size limit: a plan that splits some tiles into S pieces needs
+ *     (split tiles) * S * 256 KiB (+ 16 bytes per tile, tiles = ceil(M/256) *
  *     ceil(N/256)); if that exceeds 64 MiB the call returns
  *     EMU_STATUS_NOT_SUPPORTED and enqueues nothing.  Plans without a split
  *     use no scratch and are never rejected for size.
@@ -209,6 +209,25 @@ emu_status_t emu_sgemm_noalloc(emu_mode_t mode, emu_op_t transA, emu_op_t transB
  * EMU_STATUS_DEVICE_TIMEOUT and clears the flag.  No fault, trap or hang.
  */
 emu_status_t emu_selftest_wait_timeout(uint64_t budget_ns, emu_stream_t stream);
+
+/*
+ * emu_plan_query -- diagnostic, host only (no GPU, no CUDA call): the launch
+ * plan emu_sgemm would use for an M x N x K product on a device with `pairs`
+ * co-resident CTA pairs (76 on a GB300), honouring the EMU_SPLIT_K and
+ * EMU_PIPE overrides.  Writes EMU_PLAN_FIELDS values to out[0..]:
+ *   0 pipeline shape (0 short-k, 1 long-k)   1 tile width (256)
+ *   2 tiles along M (256 rows each)          3 tiles along N
+ *   4 k-stages (32 each)                     5 tiles processed first (tiles_a)
+ *   6 pieces per tile of those (split_a)     7 pieces per remaining tile (split_b)
+ *   8 work units                             9 CTA pairs launched
+ *  10 workspace partial tiles (256 x 256 FP32 each; 0 = no split tile)
+ * Work unit u of the first group is piece u % split_a of tile u / split_a;
+ * the remaining tiles follow, split_b units each; pair c runs units c,
+ * c + pairs launched, ...  INVALID_VALUE for non-positive sizes, pairs < 1,
+ * a NULL `out` or n < EMU_PLAN_FIELDS.
+ */
+#define EMU_PLAN_FIELDS 11
+emu_status_t emu_plan_query(int64_t M, int64_t N, int64_t K, int pairs, int64_t *out, int n);
 
 /* Library version as an integer (major * 10000 + minor * 100 + patch). */
 int emu_version(void);

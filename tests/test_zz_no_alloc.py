@@ -76,13 +76,17 @@ def test_noalloc_matches_emu_sgemm_on_two_calls(mode, case):
     _gpu.compare(mode, got, oracle.Problem(A, B), rows, elementwise=False)
 
 
-def test_noalloc_rejects_plans_beyond_its_scratch():
-    """The wide-model input gradient splits 96 tiles into 3 pieces, which needs
-    72 MiB of partial tiles: more than the 64 MiB array, so the call is
-    refused with EMU_STATUS_NOT_SUPPORTED and enqueues nothing."""
+def test_noalloc_rejects_plans_beyond_its_scratch(monkeypatch):
+    """Automatic plans keep split tiles to one wave of units (at most one
+    partial tile per CTA pair, about 19 MiB), so a plan beyond the 64 MiB
+    array is forced here: the wide-model input gradient (96 tiles, 128
+    k-stages) with every tile split into 32 pieces needs 768 MiB of partial
+    tiles.  The call is refused with EMU_STATUS_NOT_SUPPORTED and enqueues
+    nothing."""
     import torch
     import fp32_emulated_gemm_gb300 as emu
     dev = _gpu.device()
+    monkeypatch.setenv("EMU_SPLIT_K", "32")
     M, N, K = 6144, 1024, 4096  # dX = dY[6144, 4096] W[4096, 1024]
     A = torch.zeros((M, K), device=dev)
     B = torch.zeros((K, N), device=dev)
