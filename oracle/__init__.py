@@ -69,9 +69,13 @@ def lib():
             L.oracle_gemm_tf32x3.argtypes = gemm_head + [f32, P, i64, P, i64, f32, P, i64, P, i32, P, i64, P, P]
             L.oracle_gemm_bf16x6.argtypes = gemm_head + [f32, P, i64, P, i64, f32, P, i64, P, P, i64, P]
             L.oracle_gemm_tf32x1.argtypes = gemm_head + [f32, P, i64, P, i64, f32, P, i64, P, P, i64, P]
+            L.oracle_gemm_tc.argtypes = gemm_head + [f32, P, i64, P, i64, f32, P, i64, P, P, i64, P,
+                                                     i32, i32, i32, i32, i32, i32]
+            L.oracle_tc_block_fma.argtypes = [f32, P, P, i32, i32, i32]
+            L.oracle_tc_block_fma.restype = f32
             for name in ("oracle_gemm_f64", "oracle_gemm_absdenom_f64", "oracle_sgemm_f32",
                          "oracle_gemm_bf16x9", "oracle_gemm_tf32x3", "oracle_gemm_bf16x6",
-                         "oracle_gemm_tf32x1", "oracle_num_threads"):
+                         "oracle_gemm_tf32x1", "oracle_gemm_tc", "oracle_num_threads"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -92,7 +96,7 @@ class use_library:
         for name in ("oracle_split_bf16x9", "oracle_split_bf16x9_f32", "oracle_split_tf32x3",
                      "oracle_gemm_f64", "oracle_gemm_absdenom_f64", "oracle_sgemm_f32",
                      "oracle_gemm_bf16x9", "oracle_gemm_tf32x3", "oracle_gemm_bf16x6",
-                     "oracle_gemm_tf32x1", "oracle_num_threads"):
+                     "oracle_gemm_tf32x1", "oracle_gemm_tc", "oracle_tc_block_fma", "oracle_num_threads"):
             f, g = getattr(L, name), getattr(self._saved, name)
             f.argtypes, f.restype = g.argtypes, g.restype
         _lib = L
@@ -280,6 +284,42 @@ def gemm_tf32x1(p: Problem, rows=None):
                                   _ptr(p.bias), _ptr(r), nr, _ptr(out))
     if rc:
         raise MemoryError("oracle_gemm_tf32x1")
+    return out
+
+
+# Tensor-core model parameters ([TC models] "Results"): blocks of 16 products
+# for BF16 inputs (one 16-deep instruction of the kernel), 8 for TF32 (one
+# 8-deep instruction), 2 extra alignment bits, rounding toward zero.
+TC_NEAB = 2
+TC_TOWARD_ZERO, TC_NEAREST = 0, 1
+TC_KIND = {"bf16x9": 0, "bf16x6": 1, "tf32x3": 2, "tf32x1": 3}
+TC_BLOCK = {"bf16x9": 16, "bf16x6": 16, "tf32x3": 8, "tf32x1": 8}
+
+
+def tc_block_fma(c, a, b, neab=TC_NEAB, round_mode=TC_TOWARD_ZERO):
+    """One block FMA of the tensor-core model: FP32 c plus sum a_i b_i."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    b = np.ascontiguousarray(b, dtype=np.float32)
+    assert a.shape == b.shape and a.ndim == 1
+    return float(lib().oracle_tc_block_fma(float(c), _ptr(a), _ptr(b), len(a), int(neab), int(round_mode)))
+
+
+def gemm_tc(p: Problem, mode="bf16x9", rows=None, *, pieces=1, stage_k=32, block=None, neab=TC_NEAB,
+            round_mode=TC_TOWARD_ZERO):
+    """The emulated GEMM through the tensor-core accumulation model, in the
+    kernel's issue order (see oracle_gemm_tc); pieces > 1 models a split of
+    every tile's k-range into that many pieces, reduced owner first."""
+    block = TC_BLOCK[mode] if block is None else block
+    (h, lda, ldb), (r, nr) = p._head(), p._rows(rows)
+    out = np.empty((nr, p.N), np.float32)
+    cp, ldc = p._cold()
+    rc = lib().oracle_gemm_tc(*h, p.alpha, _ptr(p.A), lda, _ptr(p.B), ldb, p.beta, cp, ldc,
+                              _ptr(p.bias), _ptr(r), nr, _ptr(out), TC_KIND[mode], int(stage_k), int(block),
+                              int(neab), int(round_mode), int(pieces))
+    if rc == -2:
+        raise ValueError("gemm_tc: bad mode, block, stage or pieces")
+    if rc:
+        raise MemoryError("oracle_gemm_tc")
     return out
 
 

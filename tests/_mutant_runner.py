@@ -12,6 +12,7 @@ import oracle
 from tests import _bits
 from tests import test_oracle_gemm as g
 from tests import test_oracle_split as s
+from tests import test_oracle_tc as tc
 
 
 def run_pins():
@@ -43,6 +44,18 @@ def run_pins():
     g.test_k_zero_gives_beta_c_plus_bias()
     for seed in (0, 1, 2):
         g.test_bf16x9_meets_or_beats_native_fp32(seed)
+    # tensor-core model pins
+    tc.test_exact_sums_are_exact()
+    tc.test_alignment_uses_the_unnormalised_product_exponent()
+    tc.test_terms_are_truncated_toward_zero()
+    tc.test_block_sum_rounds_toward_zero()
+    tc.test_wide_alignment_to_nearest_is_the_correctly_rounded_sum()
+    tc.test_two_alignment_bits_lose_only_below_the_window()
+    for mode in ("bf16x9", "bf16x6", "tf32x3", "tf32x1"):
+        tc.test_bf16_exact_inputs_reduce_to_one_block_chain(mode)
+    for mode in ("bf16x9", "tf32x3"):
+        tc.test_model_within_the_stated_error_bound(mode)
+    tc.test_split_pieces_are_reduced_owner_first()
 
 
 if __name__ == "__main__":
