@@ -22,6 +22,8 @@ __all__ = [
     "EmuError",
     "emu_sgemm", "emu_linear_fwd", "emu_linear_bwd_input", "emu_linear_bwd_weight", "emu_status_string",
     "emu_stream_check", "emu_split_dump", "emu_plan_query", "emu_version",
+    "emu_pack_bytes", "emu_pack_b", "emu_sgemm_packed_b", "emu_linear_fwd_packed", "emu_linear_bwd_input_packed",
+    "pack_b", "sgemm_packed", "PackedWeight", "pack_weight", "linear_fwd_packed", "linear_bwd_input_packed",
     "sgemm", "linear_fwd", "linear_bwd_input", "linear_bwd_weight", "EmuLinearFunction", "EmuLinear",
     "library_path", "load",
 ]
@@ -76,6 +78,14 @@ def load():
         L.emu_status_string.restype = ctypes.c_char_p
         L.emu_stream_check.argtypes = [P]
         L.emu_split_dump.argtypes = [i32, i64, i64, P, i64, i32, P, P]
+        L.emu_pack_bytes.argtypes = [i32, i64, i64]
+        L.emu_pack_bytes.restype = i64
+        L.emu_pack_b.argtypes = [i32, i32, i64, i64, P, i64, P, P]
+        L.emu_sgemm_packed_b.argtypes = [i32, i32, i64, i64, i64, f32, P, i64, P, f32, P, i64, P]
+        L.emu_linear_fwd_packed.argtypes = [i32, i64, i64, i64, P, P, P, P, P]
+        L.emu_linear_bwd_input_packed.argtypes = [i32, i64, i64, i64, P, P, P, P]
+        for name in ("emu_pack_b", "emu_sgemm_packed_b", "emu_linear_fwd_packed", "emu_linear_bwd_input_packed"):
+            getattr(L, name).restype = i32
         L.emu_plan_query.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64), i32]
         L.emu_plan_query.restype = i32
         L.emu_version.argtypes = []
@@ -138,6 +148,32 @@ def emu_split_dump(mode, R, Kc, X, ldx, mn_major, out, stream=None):
                                  ctypes.c_void_p(_stream(stream))), "emu_split_dump")
 
 
+def emu_pack_bytes(mode, N, K) -> int:
+    return int(load().emu_pack_bytes(int(mode), int(N), int(K)))
+
+
+def emu_pack_b(mode, transB, N, K, B, ldb, packed, stream=None):
+    _check(load().emu_pack_b(int(mode), int(transB), int(N), int(K), _ptr(B), int(ldb), _ptr(packed),
+                             ctypes.c_void_p(_stream(stream))), "emu_pack_b")
+
+
+def emu_sgemm_packed_b(mode, transA, M, N, K, alpha, A, lda, packed_b, beta, C, ldc, stream=None):
+    _check(load().emu_sgemm_packed_b(int(mode), int(transA), int(M), int(N), int(K), float(alpha), _ptr(A),
+                                     int(lda), _ptr(packed_b), float(beta), _ptr(C), int(ldc),
+                                     ctypes.c_void_p(_stream(stream))), "emu_sgemm_packed_b")
+
+
+def emu_linear_fwd_packed(mode, M, N, K, X, W_packed, bias, Y, stream=None):
+    _check(load().emu_linear_fwd_packed(int(mode), int(M), int(N), int(K), _ptr(X), _ptr(W_packed), _ptr(bias),
+                                        _ptr(Y), ctypes.c_void_p(_stream(stream))), "emu_linear_fwd_packed")
+
+
+def emu_linear_bwd_input_packed(mode, M, N, K, dY, Wt_packed, dX, stream=None):
+    _check(load().emu_linear_bwd_input_packed(int(mode), int(M), int(N), int(K), _ptr(dY), _ptr(Wt_packed),
+                                              _ptr(dX), ctypes.c_void_p(_stream(stream))),
+           "emu_linear_bwd_input_packed")
+
+
 PLAN_FIELDS = ("pipe", "tile_n", "tiles_m", "tiles_n", "k_stages", "tiles_a", "split_a", "split_b",
                "units", "pairs", "slots")
 
@@ -167,6 +203,15 @@ def _f32_cuda(t, name):
     return t
 
 
+def _new_c(M, N, device):
+    """An M x N float32 result whose rows start on 16-byte boundaries (the
+    library wants ldc to be a multiple of 4): a view of a padded buffer when
+    N is not a multiple of 4."""
+    import torch
+    ld = (N + 3) // 4 * 4
+    return torch.empty((M, ld), device=device, dtype=torch.float32)[:, :N]
+
+
 def sgemm(A, B, *, mode="bf16x9", transA=False, transB=False, alpha=1.0, beta=0.0, C=None):
     """C = alpha op(A) op(B) + beta C on the current stream (C allocated when None)."""
     import torch
@@ -176,13 +221,73 @@ def sgemm(A, B, *, mode="bf16x9", transA=False, transB=False, alpha=1.0, beta=0.
     if Kb != K:
         raise ValueError("inner dimensions differ")
     if C is None:
-        C = torch.empty((M, N), device=A.device, dtype=torch.float32)
         if beta != 0.0:
             raise ValueError("beta != 0 needs C")
+        C = _new_c(M, N, A.device)
     _f32_cuda(C, "C")
     emu_sgemm(_mode(mode), EMU_OP_T if transA else EMU_OP_N, EMU_OP_T if transB else EMU_OP_N, M, N, K,
               alpha, A, A.stride(0), B, B.stride(0), beta, C, C.stride(0))
     return C
+
+
+def pack_b(B, *, mode="bf16x9", transB=False):
+    """Packed form of op(B) (a uint8 device tensor) for sgemm_packed."""
+    import torch
+    _f32_cuda(B, "B")
+    K, N = (B.shape[1], B.shape[0]) if transB else B.shape
+    out = torch.empty(max(1, emu_pack_bytes(_mode(mode), N, K)), dtype=torch.uint8, device=B.device)
+    emu_pack_b(_mode(mode), EMU_OP_T if transB else EMU_OP_N, N, K, B, B.stride(0), out)
+    return out
+
+
+def sgemm_packed(A, packed_b, N, *, mode="bf16x9", transA=False, alpha=1.0, beta=0.0, C=None):
+    """C = alpha op(A) op(B) + beta C with op(B) given by pack_b (N columns)."""
+    import torch
+    _f32_cuda(A, "A")
+    M, K = (A.shape[1], A.shape[0]) if transA else A.shape
+    if C is None:
+        if beta != 0.0:
+            raise ValueError("beta != 0 needs C")
+        C = _new_c(M, N, A.device)
+    _f32_cuda(C, "C")
+    emu_sgemm_packed_b(_mode(mode), EMU_OP_T if transA else EMU_OP_N, M, N, K, alpha, A, A.stride(0), packed_b,
+                       beta, C, C.stride(0))
+    return C
+
+
+class PackedWeight:
+    """A linear layer's weight W [N, K] split once for both passes: `fwd` for
+    Y = X W^T + b and `bwd` for dX = dY W.  Valid while W is unchanged (see
+    `version`, the tensor's version counter when it was packed)."""
+
+    def __init__(self, W, mode="bf16x9"):
+        _f32_cuda(W, "W")
+        W = W.contiguous()
+        self.mode, self.N, self.K = mode, W.shape[0], W.shape[1]
+        self.version = W._version
+        self.fwd = pack_b(W, mode=mode, transB=True)
+        self.bwd = pack_b(W, mode=mode, transB=False)
+
+
+def pack_weight(W, mode="bf16x9"):
+    return PackedWeight(W, mode)
+
+
+def linear_fwd_packed(X, pw: PackedWeight, bias=None, *, out=None):
+    import torch
+    M, K = X.shape
+    Y = out if out is not None else torch.empty((M, pw.N), device=X.device, dtype=torch.float32)
+    emu_linear_fwd_packed(_mode(pw.mode), M, pw.N, K, X.contiguous(), pw.fwd,
+                          None if bias is None else bias.contiguous(), Y)
+    return Y
+
+
+def linear_bwd_input_packed(dY, pw: PackedWeight, *, out=None):
+    import torch
+    M, N = dY.shape
+    dX = out if out is not None else torch.empty((M, pw.K), device=dY.device, dtype=torch.float32)
+    emu_linear_bwd_input_packed(_mode(pw.mode), M, N, pw.K, dY.contiguous(), pw.bwd, dX)
+    return dX
 
 
 def linear_fwd(X, W, bias=None, *, mode="bf16x9", out=None):
@@ -225,18 +330,24 @@ def _autograd():
         TF32Linear ("TF32x3 on Ampere GPUs"), unless weight_grad="emulated"."""
 
         @staticmethod
-        def forward(ctx, X, W, bias, mode, weight_grad="fp32"):
+        def forward(ctx, X, W, bias, mode, weight_grad="fp32", packed=None):
             ctx.save_for_backward(X, W)
             ctx.mode = mode
             ctx.weight_grad = weight_grad
             ctx.has_bias = bias is not None
+            ctx.packed = packed
+            if packed is not None:
+                return linear_fwd_packed(X, packed, bias)
             return linear_fwd(X, W, bias, mode=mode)
 
         @staticmethod
         def backward(ctx, dY):
             X, W = ctx.saved_tensors
             dY = dY.contiguous()
-            dX = linear_bwd_input(dY, W, mode=ctx.mode) if ctx.needs_input_grad[0] else None
+            dX = None
+            if ctx.needs_input_grad[0]:
+                dX = (linear_bwd_input_packed(dY, ctx.packed) if ctx.packed is not None
+                      else linear_bwd_input(dY, W, mode=ctx.mode))
             dW = db = None
             if ctx.needs_input_grad[1] and ctx.weight_grad == "emulated":
                 dW = linear_bwd_weight(dY, X, mode=ctx.mode)
@@ -249,20 +360,37 @@ def _autograd():
                     torch.backends.cuda.matmul.allow_tf32 = prev
             if ctx.has_bias and ctx.needs_input_grad[2]:
                 db = dY.sum(0)
-            return dX, dW, db, None, None
+            return dX, dW, db, None, None, None
 
     class EmuLinear(torch.nn.Linear):
         """Drop-in nn.Linear whose matmuls run on the emulated path."""
 
-        def __init__(self, in_features, out_features, bias=True, mode="bf16x9", weight_grad="fp32", **kw):
+        def __init__(self, in_features, out_features, bias=True, mode="bf16x9", weight_grad="fp32",
+                     prepack=False, **kw):
+            """prepack=True splits the weight once and reuses the split until the
+            weight changes (fixed-weight inference and molecular dynamics)."""
             super().__init__(in_features, out_features, bias=bias, **kw)
             self.mode = mode
             self.weight_grad = weight_grad
+            self.prepack = prepack
+            self._packed = None
+
+        def _packed_weight(self):
+            W = self.weight
+            pw = self._packed
+            if (pw is None or pw.version != W._version or pw.mode != self.mode or pw.N != W.shape[0]
+                    or pw.K != W.shape[1] or pw.fwd.device != W.device):
+                with torch.no_grad():
+                    pw = PackedWeight(W.detach(), self.mode)
+                pw.version = W._version
+                self._packed = pw
+            return pw
 
         def forward(self, x):
             shp = x.shape
+            packed = self._packed_weight() if self.prepack else None
             y = EmuLinearFunction.apply(x.reshape(-1, shp[-1]), self.weight, self.bias, self.mode,
-                                        self.weight_grad)
+                                        self.weight_grad, packed)
             return y.reshape(*shp[:-1], self.out_features)
 
     return EmuLinearFunction, EmuLinear

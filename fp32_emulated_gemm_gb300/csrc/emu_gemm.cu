@@ -126,7 +126,13 @@ emu_status_t device_info(DeviceInfo** out) {
             set_smem_attr<MODE_BF16X6, PIPE_SHORT_K>() != cudaSuccess ||
             set_smem_attr<MODE_BF16X6, PIPE_LONG_K>() != cudaSuccess ||
             set_smem_attr<MODE_TF32X3, PIPE_SHORT_K>() != cudaSuccess ||
-            set_smem_attr<MODE_TF32X1, PIPE_SHORT_K>() != cudaSuccess) {
+            set_smem_attr<MODE_TF32X1, PIPE_SHORT_K>() != cudaSuccess ||
+            set_smem_attr<MODE_BF16X9, PIPE_SHORT_K_PACKED>() != cudaSuccess ||
+            set_smem_attr<MODE_BF16X9, PIPE_LONG_K_PACKED>() != cudaSuccess ||
+            set_smem_attr<MODE_BF16X6, PIPE_SHORT_K_PACKED>() != cudaSuccess ||
+            set_smem_attr<MODE_BF16X6, PIPE_LONG_K_PACKED>() != cudaSuccess ||
+            set_smem_attr<MODE_TF32X3, PIPE_SHORT_K_PACKED>() != cudaSuccess ||
+            set_smem_attr<MODE_TF32X1, PIPE_SHORT_K_PACKED>() != cudaSuccess) {
             cudaGetLastError();
             return EMU_STATUS_LAUNCH_FAILED;
         }
@@ -184,6 +190,75 @@ bool encode_operand(CUtensorMap* map, const float* X, bool mn_major, int64_t MN,
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Packed op(B) (emu_pack_b): the components of op(B)^T, one plane per
+// component, each `rows` rows of Kp = K rounded up to 32 elements, zero past
+// K: BF16 words for the BF16 modes, FP32 words (TF32 values) for the TF32
+// modes.  A stage's box of a plane lands in shared memory in the kernel's
+// component layout (64-byte BF16 rows with the 64-byte swizzle, 128-byte TF32
+// rows with the 128-byte swizzle).
+int ncomp_of(emu_mode_t mode) { return mode == EMU_MODE_TF32X3 ? 2 : mode == EMU_MODE_TF32X1 ? 1 : 3; }
+int64_t elem_bytes_of(emu_mode_t mode) { return mode == EMU_MODE_TF32X3 || mode == EMU_MODE_TF32X1 ? 4 : 2; }
+__host__ __device__ inline int64_t packed_kp(int64_t K) { return (K + BK - 1) / BK * BK; }
+int64_t packed_bytes(emu_mode_t mode, int64_t rows, int64_t K) {
+    return ncomp_of(mode) * rows * packed_kp(K) * elem_bytes_of(mode);
+}
+
+bool encode_packed(CUtensorMap* map, const void* packed, emu_mode_t mode, int64_t rows, int64_t K) {
+    const int64_t es = elem_bytes_of(mode), kp = packed_kp(K);
+    const cuuint64_t dims[3] = {(cuuint64_t)kp, (cuuint64_t)rows, (cuuint64_t)ncomp_of(mode)};
+    const cuuint64_t strides[2] = {(cuuint64_t)(kp * es), (cuuint64_t)(rows * kp * es)};
+    const cuuint32_t box[3] = {BK, (cuuint32_t)(TILE_M / 2), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(map, es == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                                const_cast<void*>(packed), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                es == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS && log_enabled())
+        std::fprintf(stderr, "[emu] packed tensor map encode failed (%d): rows %lld K %lld\n", (int)r,
+                     (long long)rows, (long long)K);
+    return r == CUDA_SUCCESS;
+}
+
+// One thread per (row of op(B)^T, 8 consecutive k): the kernel's own split
+// of those 8 values, written to every plane.
+template <int MODE>
+__global__ void pack_kernel(int64_t rows, int64_t K, const float* B, int64_t ldb, int b_k_major, void* packed) {
+    using C = Cfg<MODE>;
+    const int64_t kp = packed_kp(K), groups = kp / 8, total = rows * groups;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t n = i / groups, k0 = (i % groups) * 8;
+        float x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int64_t k = k0 + j;
+            x[j] = k < K ? (b_k_major ? B[n * ldb + k] : B[k * ldb + n]) : 0.0f;
+        }
+        const int64_t plane = rows * kp;  // elements per plane
+        if constexpr (!C::TF32) {
+            uint4 s0, s1, s2;
+            split_bf16x9_8(x, s0, s1, s2);
+            uint16_t* out = reinterpret_cast<uint16_t*>(packed) + n * kp + k0;
+            *reinterpret_cast<uint4*>(out) = s0;
+            *reinterpret_cast<uint4*>(out + plane) = s1;
+            *reinterpret_cast<uint4*>(out + 2 * plane) = s2;
+        } else {
+            uint32_t h[8], l[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if constexpr (C::NCOMP == 2) split_tf32x3_1(x[j], h[j], l[j]);
+                else h[j] = tf32_rn_bits(__float_as_uint(x[j]));
+            }
+            uint32_t* out = reinterpret_cast<uint32_t*>(packed) + n * kp + k0;
+            *reinterpret_cast<uint4*>(out) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(out + 4) = make_uint4(h[4], h[5], h[6], h[7]);
+            if constexpr (C::NCOMP == 2) {
+                *reinterpret_cast<uint4*>(out + plane) = make_uint4(l[0], l[1], l[2], l[3]);
+                *reinterpret_cast<uint4*>(out + plane + 4) = make_uint4(l[4], l[5], l[6], l[7]);
+            }
+        }
+    }
+}
 
 __global__ void scale_kernel(int64_t M, int64_t N, float beta, float* C, int64_t ldc, const float* bias) {
     const int64_t total = M * N;
@@ -374,16 +449,24 @@ cudaError_t launch_gemm(emu_mode_t mode, int pipe, const Params& p, int clusters
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    const bool long_k = pipe == PIPE_LONG_K;
+    const bool long_k = pipe == PIPE_LONG_K || pipe == PIPE_LONG_K_PACKED, packed = pipe_packed(pipe);
     cudaError_t e;
     switch (mode) {
-        case EMU_MODE_TF32X3: e = launch_one<MODE_TF32X3, PIPE_SHORT_K>(cfg, p); break;
-        case EMU_MODE_TF32X1: e = launch_one<MODE_TF32X1, PIPE_SHORT_K>(cfg, p); break;
+        case EMU_MODE_TF32X3:
+            e = packed ? launch_one<MODE_TF32X3, PIPE_SHORT_K_PACKED>(cfg, p) : launch_one<MODE_TF32X3, PIPE_SHORT_K>(cfg, p);
+            break;
+        case EMU_MODE_TF32X1:
+            e = packed ? launch_one<MODE_TF32X1, PIPE_SHORT_K_PACKED>(cfg, p) : launch_one<MODE_TF32X1, PIPE_SHORT_K>(cfg, p);
+            break;
         case EMU_MODE_BF16X6:
-            e = long_k ? launch_one<MODE_BF16X6, PIPE_LONG_K>(cfg, p) : launch_one<MODE_BF16X6, PIPE_SHORT_K>(cfg, p);
+            e = packed ? (long_k ? launch_one<MODE_BF16X6, PIPE_LONG_K_PACKED>(cfg, p)
+                                 : launch_one<MODE_BF16X6, PIPE_SHORT_K_PACKED>(cfg, p))
+                       : (long_k ? launch_one<MODE_BF16X6, PIPE_LONG_K>(cfg, p) : launch_one<MODE_BF16X6, PIPE_SHORT_K>(cfg, p));
             break;
         default:
-            e = long_k ? launch_one<MODE_BF16X9, PIPE_LONG_K>(cfg, p) : launch_one<MODE_BF16X9, PIPE_SHORT_K>(cfg, p);
+            e = packed ? (long_k ? launch_one<MODE_BF16X9, PIPE_LONG_K_PACKED>(cfg, p)
+                                 : launch_one<MODE_BF16X9, PIPE_SHORT_K_PACKED>(cfg, p))
+                       : (long_k ? launch_one<MODE_BF16X9, PIPE_LONG_K>(cfg, p) : launch_one<MODE_BF16X9, PIPE_SHORT_K>(cfg, p));
     }
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -393,9 +476,10 @@ cudaError_t launch_gemm(emu_mode_t mode, int pipe, const Params& p, int clusters
 }
 
 // Core: C = alpha * op(A) op(B) + beta * C_old + bias, with C_old == C.
+// packed_b != nullptr: op(B) comes packed (emu_pack_b); B and ldb are unused.
 emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t N, int64_t K, float alpha,
                       const float* A, int64_t lda, const float* B, int64_t ldb, float beta, float* C,
-                      int64_t ldc, const float* bias, cudaStream_t stream) {
+                      int64_t ldc, const float* bias, cudaStream_t stream, const void* packed_b = nullptr) {
     if (!valid_mode(mode)) return EMU_STATUS_INVALID_VALUE;
     if (M < 0 || N < 0 || K < 0) return EMU_STATUS_INVALID_VALUE;
     if (M > INT32_MAX - 256 || N > INT32_MAX - 256 || K > INT32_MAX - 256) return EMU_STATUS_NOT_SUPPORTED;
@@ -405,7 +489,10 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
     (void)a_rows; (void)b_rows;
     if (ldc < N || !C) return EMU_STATUS_INVALID_VALUE;
     const bool gemm = K > 0 && alpha != 0.0f;
-    if (gemm) {
+    if (gemm && packed_b) {
+        if (!A || lda < a_cols) return EMU_STATUS_INVALID_VALUE;
+        if (!aligned16(A) || !aligned16(packed_b) || (lda & 3)) return EMU_STATUS_NOT_SUPPORTED;
+    } else if (gemm) {
         if (!A || !B || lda < a_cols || ldb < b_cols) return EMU_STATUS_INVALID_VALUE;
         if (!aligned16(A) || !aligned16(B) || (lda & 3) || (ldb & 3)) return EMU_STATUS_NOT_SUPPORTED;
     }
@@ -427,13 +514,15 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
     }
 
     const int pairs = dev->max_clusters[mode == EMU_MODE_TF32X3 ? 1 : 0];
-    const Plan plan = make_plan(M, N, K, pairs);
+    Plan plan = make_plan(M, N, K, pairs);
+    if (packed_b) plan.pipe = plan.pipe == PIPE_LONG_K ? PIPE_LONG_K_PACKED : PIPE_SHORT_K_PACKED;
     Params p{};
     if (!encode_operand(&p.tmA, A, a_mn, M, K, lda, HALF) ||
-        !encode_operand(&p.tmB, B, b_mn, N, K, ldb, (uint32_t)plan.tn / 2))
+        !(packed_b ? encode_packed(&p.tmB, packed_b, mode, N, K)
+                   : encode_operand(&p.tmB, B, b_mn, N, K, ldb, (uint32_t)plan.tn / 2)))
         return EMU_STATUS_LAUNCH_FAILED;
     p.M = (int)M; p.N = (int)N; p.K = (int)K;
-    p.a_mn_major = a_mn; p.b_mn_major = b_mn;
+    p.a_mn_major = a_mn; p.b_mn_major = packed_b ? 0 : b_mn;
     p.tiles_m = plan.tiles_m;
     p.tiles_n = plan.tiles_n;
     p.num_tiles = plan.num_tiles;
@@ -561,6 +650,60 @@ emu_status_t emu_linear_bwd_weight(emu_mode_t mode, int64_t M, int64_t N, int64_
     // operands are MN-major (their rows are the contraction index)
     return run_gemm(mode, true, true, N, K, M, 1.0f, dY, N, X, K, beta, dW, K, nullptr,
                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+int64_t emu_pack_bytes(emu_mode_t mode, int64_t N, int64_t K) {
+    if (!valid_mode(mode) || N < 0 || K < 0) return -1;
+    return packed_bytes(mode, N, K);
+}
+
+emu_status_t emu_pack_b(emu_mode_t mode, emu_op_t transB, int64_t N, int64_t K, const float* B, int64_t ldb,
+                        void* packed, emu_stream_t stream) {
+    if (!valid_mode(mode) || (transB != EMU_OP_N && transB != EMU_OP_T)) return EMU_STATUS_INVALID_VALUE;
+    if (N < 0 || K < 0) return EMU_STATUS_INVALID_VALUE;
+    if (N > INT32_MAX - 256 || K > INT32_MAX - 256) return EMU_STATUS_NOT_SUPPORTED;
+    if (N == 0 || K == 0) return EMU_STATUS_SUCCESS;
+    const bool k_major = transB == EMU_OP_T;  // op(B)^T rows are B's rows when B is stored N x K
+    if (!B || !packed || ldb < (k_major ? K : N)) return EMU_STATUS_INVALID_VALUE;
+    if (!aligned16(packed)) return EMU_STATUS_NOT_SUPPORTED;
+    DeviceInfo* dev = nullptr;
+    emu_status_t st = device_info(&dev);
+    if (st != EMU_STATUS_SUCCESS) return st;
+    const int64_t items = N * (packed_kp(K) / 8);
+    const int threads = 256;
+    const int64_t blocks64 = (items + threads - 1) / threads;
+    const int blocks = (int)(blocks64 < dev->sm_count * 16 ? blocks64 : dev->sm_count * 16);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaGetLastError();
+    switch (mode) {
+        case EMU_MODE_TF32X3: pack_kernel<MODE_TF32X3><<<blocks, threads, 0, s>>>(N, K, B, ldb, k_major, packed); break;
+        case EMU_MODE_TF32X1: pack_kernel<MODE_TF32X1><<<blocks, threads, 0, s>>>(N, K, B, ldb, k_major, packed); break;
+        default: pack_kernel<MODE_BF16X9><<<blocks, threads, 0, s>>>(N, K, B, ldb, k_major, packed);  // BF16x6 too
+    }
+    return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
+}
+
+emu_status_t emu_sgemm_packed_b(emu_mode_t mode, emu_op_t transA, int64_t M, int64_t N, int64_t K, float alpha,
+                                const float* A, int64_t lda, const void* packed_b, float beta, float* C,
+                                int64_t ldc, emu_stream_t stream) {
+    if (transA != EMU_OP_N && transA != EMU_OP_T) return EMU_STATUS_INVALID_VALUE;
+    if (!packed_b && K > 0 && alpha != 0.0f) return EMU_STATUS_INVALID_VALUE;
+    return run_gemm(mode, transA == EMU_OP_T, false, M, N, K, alpha, A, lda, nullptr, 0, beta, C, ldc, nullptr,
+                    reinterpret_cast<cudaStream_t>(stream), packed_b);
+}
+
+emu_status_t emu_linear_fwd_packed(emu_mode_t mode, int64_t M, int64_t N, int64_t K, const float* X,
+                                   const void* W_packed, const float* bias, float* Y, emu_stream_t stream) {
+    if (!W_packed && K > 0) return EMU_STATUS_INVALID_VALUE;
+    return run_gemm(mode, false, false, M, N, K, 1.0f, X, K, nullptr, 0, 0.0f, Y, N, bias,
+                    reinterpret_cast<cudaStream_t>(stream), W_packed);
+}
+
+emu_status_t emu_linear_bwd_input_packed(emu_mode_t mode, int64_t M, int64_t N, int64_t K, const float* dY,
+                                         const void* Wt_packed, float* dX, emu_stream_t stream) {
+    if (!Wt_packed && N > 0) return EMU_STATUS_INVALID_VALUE;
+    return run_gemm(mode, false, false, M, K, N, 1.0f, dY, N, nullptr, 0, 0.0f, dX, K, nullptr,
+                    reinterpret_cast<cudaStream_t>(stream), Wt_packed);
 }
 
 const char* emu_status_string(emu_status_t s) {

@@ -127,20 +127,36 @@ template <> struct Cfg<MODE_TF32X1> : CfgTF32 {
 // was measured slower on every workload: the kernel is bound by
 // shared-memory bandwidth (about 90 bytes per clock per SM sustained), and
 // halving the tile width raises the operand bytes per product by half.
-enum Pipe : int { PIPE_SHORT_K = 0, PIPE_LONG_K = 1 };
+enum Pipe : int { PIPE_SHORT_K = 0, PIPE_LONG_K = 1, PIPE_SHORT_K_PACKED = 2, PIPE_LONG_K_PACKED = 3 };
+constexpr bool pipe_packed(int pipe) { return pipe >= PIPE_SHORT_K_PACKED; }
+// The *_PACKED shapes take op(B) already split (emu_pack_b): its component
+// tiles come by TMA straight into the component ring, the FP32 ring holds
+// op(A) alone and the split warps split op(A) alone.
 template <int MODE, int PIPE> struct PipeCfg;
 template <> struct PipeCfg<MODE_BF16X9, PIPE_SHORT_K> {
     static constexpr int TN = 256, NF = 3, NS = 2, OUT_COLS = 32;
+    static constexpr bool PACKED = false;
 };
 template <> struct PipeCfg<MODE_BF16X9, PIPE_LONG_K> {
     static constexpr int TN = 256, NF = 2, NS = 3, OUT_COLS = 16;
+    static constexpr bool PACKED = false;
+};
+template <> struct PipeCfg<MODE_BF16X9, PIPE_SHORT_K_PACKED> {
+    static constexpr int TN = 256, NF = 3, NS = 3, OUT_COLS = 32;
+    static constexpr bool PACKED = true;
+};
+template <> struct PipeCfg<MODE_BF16X9, PIPE_LONG_K_PACKED> {
+    static constexpr int TN = 256, NF = 4, NS = 3, OUT_COLS = 16;
+    static constexpr bool PACKED = true;
 };
 template <int PIPE> struct PipeCfg<MODE_BF16X6, PIPE> : PipeCfg<MODE_BF16X9, PIPE> {};
 template <int PIPE> struct PipeCfg<MODE_TF32X3, PIPE> {
-    static constexpr int TN = 256, NF = 2, NS = 2, OUT_COLS = 32;
+    static constexpr bool PACKED = pipe_packed(PIPE);
+    static constexpr int TN = 256, NF = PACKED ? 3 : 2, NS = 2, OUT_COLS = 32;
 };
 template <int PIPE> struct PipeCfg<MODE_TF32X1, PIPE> {
-    static constexpr int TN = 256, NF = 3, NS = 3, OUT_COLS = 32;
+    static constexpr bool PACKED = pipe_packed(PIPE);
+    static constexpr int TN = 256, NF = 3, NS = PACKED ? 4 : 3, OUT_COLS = 32;
 };
 
 // Everything the kernel derives from (mode, shape).
@@ -152,11 +168,13 @@ template <int MODE, int PIPE> struct KCfg {
     static constexpr int NACC = TMEM_COLS / TN;        // TMEM accumulators
     static constexpr int ACC = TN / 2;                 // accumulator registers per epilogue thread
     static constexpr int NF = P::NF, NS = P::NS, OUT_COLS = P::OUT_COLS;
+    static constexpr bool PACKED = P::PACKED;
     static constexpr uint32_t FP32_B_BYTES = BH * BK * 4;
-    static constexpr uint32_t FP32_STAGE = FP32_TILE_BYTES + FP32_B_BYTES;
+    static constexpr uint32_t FP32_STAGE = FP32_TILE_BYTES + (PACKED ? 0u : FP32_B_BYTES);
     static constexpr uint32_t COMP_A = C::COMP_TILE;                  // one component of op(A)
     static constexpr uint32_t COMP_B = BH * C::ROW_BYTES;             // one component of op(B)
     static constexpr uint32_t SLICE_STAGE = C::NCOMP * (COMP_A + COMP_B);
+    static constexpr uint32_t BCOMP_BYTES = C::NCOMP * COMP_B;        // op(B)'s components of a stage
     static constexpr uint32_t IDESC = make_idesc(C::KIND, TILE_M, TN);
     static constexpr uint32_t STAGE_OUT = 32 * OUT_COLS * 4;          // one epilogue warp's staging block
     static constexpr uint32_t SMEM = 1024 /* alignment slack */ + NF * FP32_STAGE + NS * SLICE_STAGE +
@@ -170,7 +188,8 @@ constexpr uint32_t smem_bytes() { return KCfg<MODE, PIPE>::SMEM; }
 
 struct Params {
     CUtensorMap tmA;  // FP32 op(A): K-major box {32, 128} or MN-major box {32, 32}
-    CUtensorMap tmB;  // FP32 op(B): K-major box {32, TN / 2} or MN-major box {32, 32}
+    CUtensorMap tmB;  // FP32 op(B): K-major box {32, TN / 2} or MN-major box {32, 32};
+                      // packed shapes: op(B)^T's component planes, box {32, TN / 2, 1}
     int M, N, K;
     int a_mn_major, b_mn_major;
     int tiles_m, tiles_n, num_tiles, k_stages;
@@ -369,6 +388,7 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
     using KC = KCfg<MODE, PIPE>;
     constexpr int NF = KC::NF, NS = KC::NS, OUT_COLS = KC::OUT_COLS;
     constexpr int TN = KC::TN, BH = KC::BH, NACC = KC::NACC, ACC = KC::ACC;
+    constexpr bool PACKED = KC::PACKED;
     constexpr uint32_t STAGE_OUT_BYTES = KC::STAGE_OUT;  // one epilogue warp's 32 x OUT_COLS block
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // pointer arithmetic on the shared array (not an integer round trip) keeps
@@ -386,7 +406,8 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
     uint64_t* acc_full = slice_empty + NS;    // multicast commit
     uint64_t* acc_empty = acc_full + NACC;    // leader: both CTAs' epilogue warps
     uint64_t* drain = acc_empty + NACC;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* bcomp_full = drain + 1;          // packed shapes: a stage's op(B) components landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bcomp_full + NS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
@@ -414,10 +435,21 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         const int k0 = ks * BK;
         if (!p.a_mn_major) tma_load_2d(dA, &p.tmA, full, k0, m0);
         else for (int j = 0; j < HALF / 32; ++j) tma_load_2d(dA + j * 4096, &p.tmA, full, m0 + 32 * j, k0);
-        if (!p.b_mn_major) tma_load_2d(dB, &p.tmB, full, k0, n0);
-        else for (int j = 0; j < BH / 32; ++j) tma_load_2d(dB + j * 4096, &p.tmB, full, n0 + 32 * j, k0);
+        if constexpr (!PACKED) {
+            if (!p.b_mn_major) tma_load_2d(dB, &p.tmB, full, k0, n0);
+            else for (int j = 0; j < BH / 32; ++j) tma_load_2d(dB + j * 4096, &p.tmB, full, n0 + 32 * j, k0);
+        }
     };
-    int early = 0;  // stages already issued by thread 0 (warp 0 lane 0, the producer)
+    // packed shapes: op(B)'s component tiles of a stage, straight into the
+    // component ring (box {32 k, BH rows, 1 component} per component)
+    auto issue_bload = [&](int ss, int tile, int ks) {
+        const int n0 = (tile % p.tiles_n) * TN + BH * rank;
+        uint64_t* full = &bcomp_full[ss];
+        mbar_arrive_expect_tx(full, KC::BCOMP_BYTES);
+        uint8_t* dst = slice_ring + ss * KC::SLICE_STAGE + C::NCOMP * KC::COMP_A;
+        for (int c = 0; c < C::NCOMP; ++c) tma_load_3d(dst + c * KC::COMP_B, &p.tmB, full, ks * BK, n0, c);
+    };
+    int early = 0, early_b = 0;  // stages already issued by thread 0 (warp 0 lane 0, the producer)
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&p.tmA);
         tma_prefetch_desc(&p.tmB);
@@ -425,12 +457,17 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         for (int s = 0; s < NS; ++s) { mbar_init(&slice_full[s], 2); mbar_init(&slice_empty[s], 1); }
         for (int b = 0; b < NACC; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 2); }
         mbar_init(drain, 1);
+        for (int s = 0; s < NS; ++s) mbar_init(&bcomp_full[s], 1);
         *abort_flag = 0;
         fence_mbar_init();
         griddep_wait();
-        for (int u = cid; early < NF && u < p.num_units; u += ncl) {
+        const int early_bmax = PACKED ? NS : 0;
+        for (int u = cid; (early < NF || early_b < early_bmax) && u < p.num_units; u += ncl) {
             const Unit w = unit_of(p, u);
-            for (int ks = w.kb; early < NF && ks < w.ke; ++ks, ++early) issue_load(early, w.tile, ks);
+            for (int ks = w.kb; (early < NF || early_b < early_bmax) && ks < w.ke; ++ks) {
+                if (early < NF) issue_load(early++, w.tile, ks);
+                if (early_b < early_bmax) issue_bload(early_b++, w.tile, ks);
+            }
         }
     }
     if (warp == WARP_MMA) {
@@ -449,8 +486,9 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         // ------------------------------------------------------ producer ----
         setmaxnreg_dec72();
         if (lane == 0) {
-            int s = 0, n = 0;
+            int s = 0, n = 0, bs = 0;
             uint32_t ph = 0, issued_mask = 0, issued_parity = 0;
+            uint32_t bph = 0, bissued_mask = 0, bissued_parity = 0;
             bool ok = true;
             for (int u = cid; ok && u < p.num_units; u += ncl) {
                 const Unit w = unit_of(p, u);
@@ -462,6 +500,15 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                     issued_mask |= 1u << s;
                     issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
                     if (++s == NF) { s = 0; ph ^= 1u; }
+                    if constexpr (PACKED) {
+                        if (n >= early_b) {  // the component slot is free once its MMAs are done
+                            if (!mbar_wait(&slice_empty[bs], bph ^ 1u, abort_flag, budget, 1)) { ok = false; break; }
+                            issue_bload(bs, w.tile, ks);
+                        }
+                        bissued_mask |= 1u << bs;
+                        bissued_parity = (bissued_parity & ~(1u << bs)) | (bph << bs);
+                        if (++bs == NS) { bs = 0; bph ^= 1u; }
+                    }
                 }
             }
             if (!ok) {
@@ -470,6 +517,11 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                     if (issued_mask & (1u << t)) {
                         volatile int never = 0;
                         mbar_wait(&fp32_full[t], (issued_parity >> t) & 1u, &never, 50000000ull, 1);
+                    }
+                for (int t = 0; t < NS; ++t)
+                    if (bissued_mask & (1u << t)) {
+                        volatile int never = 0;
+                        mbar_wait(&bcomp_full[t], (bissued_parity >> t) & 1u, &never, 50000000ull, 1);
                     }
             }
         }
@@ -521,8 +573,12 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                 const uint8_t* src = fp32_ring + fs * KC::FP32_STAGE;
                 uint8_t* dst = slice_ring + ss * KC::SLICE_STAGE;
                 split_operand<MODE, NUM_SPLIT_THREADS, HALF>(src, dst, p.a_mn_major != 0, t);
-                split_operand<MODE, NUM_SPLIT_THREADS, BH>(src + FP32_TILE_BYTES, dst + C::NCOMP * KC::COMP_A,
-                                                           p.b_mn_major != 0, t);
+                if constexpr (!PACKED) {
+                    split_operand<MODE, NUM_SPLIT_THREADS, BH>(src + FP32_TILE_BYTES, dst + C::NCOMP * KC::COMP_A,
+                                                               p.b_mn_major != 0, t);
+                } else {  // op(B)'s components come by TMA into the same slot
+                    if (!mbar_wait_warp(&bcomp_full[ss], sph, abort_flag, budget, 3)) { ok = false; break; }
+                }
                 // one signal per CTA: the split threads meet, then a single
                 // thread releases the stage (a cluster-scope arrive is costly)
                 fence_proxy_async_smem();

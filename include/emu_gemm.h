@@ -135,6 +135,49 @@ emu_status_t emu_linear_bwd_weight(emu_mode_t mode, int64_t M, int64_t N, int64_
                                    const float *dY, const float *X, float beta, float *dW,
                                    emu_stream_t stream);
 
+/*
+ * Weight pre-split ("packing") for fixed operands -- inference and
+ * molecular dynamics, where a layer's weights do not change between calls:
+ * the operand is split into the mode's components once, and later products
+ * load the components directly (no per-call split of that operand, fewer
+ * shared-memory bytes per k-stage).  Results are the same bits as the
+ * unpacked calls.  The blog describes the cuBLAS "performant" strategy
+ * ("BF16x9 on Blackwell GPUs"); splitting a fixed weight once is this
+ * library's form of saving per-call work.
+ *
+ * emu_pack_bytes -- device bytes a packed op(B) of N x K (output width N,
+ *   contraction K) takes in `mode`: ncomp * N * Kp * elem, Kp = K rounded up
+ *   to 32, elem 2 (BF16 modes) or 4 (TF32 modes), ncomp 3 / 2 / 1.  -1 for an
+ *   invalid mode or negative size.
+ * emu_pack_b -- write the packed form of op(B) (K x N; transB as in
+ *   emu_sgemm, B row-major with leading dimension ldb, device memory) to
+ *   `packed` (device memory, emu_pack_bytes bytes, 16-byte aligned,
+ *   caller-owned).  Layout: component planes of op(B)^T, N rows of Kp
+ *   elements each (zero past K).  Asynchronous on `stream`.
+ * emu_sgemm_packed_b -- C = alpha * op(A) * packed(op(B)) + beta * C; the
+ *   other arguments as emu_sgemm; `packed_b` made by emu_pack_b with the
+ *   same mode, N and K.
+ * emu_linear_fwd_packed -- Y = X W^T + bias with W packed by
+ *   emu_pack_b(mode, EMU_OP_T, N, K, W, K, ...).
+ * emu_linear_bwd_input_packed -- dX = dY W with W packed by
+ *   emu_pack_b(mode, EMU_OP_N, K, N, W, K, ...) (output width K,
+ *   contraction N).
+ * A packed buffer carries no header: passing one made for another mode, N or
+ * K gives wrong results (or reads past it), not an error.
+ */
+int64_t emu_pack_bytes(emu_mode_t mode, int64_t N, int64_t K);
+emu_status_t emu_pack_b(emu_mode_t mode, emu_op_t transB, int64_t N, int64_t K, const float *B,
+                        int64_t ldb, void *packed, emu_stream_t stream);
+emu_status_t emu_sgemm_packed_b(emu_mode_t mode, emu_op_t transA, int64_t M, int64_t N, int64_t K,
+                                float alpha, const float *A, int64_t lda, const void *packed_b,
+                                float beta, float *C, int64_t ldc, emu_stream_t stream);
+emu_status_t emu_linear_fwd_packed(emu_mode_t mode, int64_t M, int64_t N, int64_t K, const float *X,
+                                   const void *W_packed, const float *bias, float *Y,
+                                   emu_stream_t stream);
+emu_status_t emu_linear_bwd_input_packed(emu_mode_t mode, int64_t M, int64_t N, int64_t K,
+                                         const float *dY, const void *Wt_packed, float *dX,
+                                         emu_stream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *emu_status_string(emu_status_t s);
 
