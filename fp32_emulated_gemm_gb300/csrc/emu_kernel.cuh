@@ -130,33 +130,35 @@ template <> struct Cfg<MODE_TF32X1> : CfgTF32 {
 enum Pipe : int { PIPE_SHORT_K = 0, PIPE_LONG_K = 1, PIPE_SHORT_K_PACKED = 2, PIPE_LONG_K_PACKED = 3 };
 constexpr bool pipe_packed(int pipe) { return pipe >= PIPE_SHORT_K_PACKED; }
 // The *_PACKED shapes take op(B) already split (emu_pack_b): its component
-// tiles come by TMA straight into the component ring, the FP32 ring holds
-// op(A) alone and the split warps split op(A) alone.
+// tiles come by TMA straight into a ring of their own (NB stages, refilled as
+// soon as a stage's MMAs are done, so they arrive well ahead); the FP32 ring
+// holds op(A) alone, the component ring op(A)'s components, and the split
+// warps split op(A) alone.
 template <int MODE, int PIPE> struct PipeCfg;
 template <> struct PipeCfg<MODE_BF16X9, PIPE_SHORT_K> {
-    static constexpr int TN = 256, NF = 3, NS = 2, OUT_COLS = 32;
+    static constexpr int TN = 256, NF = 3, NS = 2, NB = 0, OUT_COLS = 32;
     static constexpr bool PACKED = false;
 };
 template <> struct PipeCfg<MODE_BF16X9, PIPE_LONG_K> {
-    static constexpr int TN = 256, NF = 2, NS = 3, OUT_COLS = 16;
+    static constexpr int TN = 256, NF = 2, NS = 3, NB = 0, OUT_COLS = 16;
     static constexpr bool PACKED = false;
 };
 template <> struct PipeCfg<MODE_BF16X9, PIPE_SHORT_K_PACKED> {
-    static constexpr int TN = 256, NF = 3, NS = 3, OUT_COLS = 32;
+    static constexpr int TN = 256, NF = 3, NS = 3, NB = 3, OUT_COLS = 32;
     static constexpr bool PACKED = true;
 };
 template <> struct PipeCfg<MODE_BF16X9, PIPE_LONG_K_PACKED> {
-    static constexpr int TN = 256, NF = 4, NS = 3, OUT_COLS = 16;
+    static constexpr int TN = 256, NF = 2, NS = 3, NB = 4, OUT_COLS = 16;
     static constexpr bool PACKED = true;
 };
 template <int PIPE> struct PipeCfg<MODE_BF16X6, PIPE> : PipeCfg<MODE_BF16X9, PIPE> {};
 template <int PIPE> struct PipeCfg<MODE_TF32X3, PIPE> {
     static constexpr bool PACKED = pipe_packed(PIPE);
-    static constexpr int TN = 256, NF = PACKED ? 3 : 2, NS = 2, OUT_COLS = 32;
+    static constexpr int TN = 256, NF = 2, NS = 2, NB = PACKED ? 3 : 0, OUT_COLS = 32;
 };
 template <int PIPE> struct PipeCfg<MODE_TF32X1, PIPE> {
     static constexpr bool PACKED = pipe_packed(PIPE);
-    static constexpr int TN = 256, NF = 3, NS = PACKED ? 4 : 3, OUT_COLS = 32;
+    static constexpr int TN = 256, NF = 3, NS = 3, NB = PACKED ? 4 : 0, OUT_COLS = 32;
 };
 
 // Everything the kernel derives from (mode, shape).
@@ -167,18 +169,19 @@ template <int MODE, int PIPE> struct KCfg {
     static constexpr int BH = TN / 2;                  // rows of op(B)^T per CTA
     static constexpr int NACC = TMEM_COLS / TN;        // TMEM accumulators
     static constexpr int ACC = TN / 2;                 // accumulator registers per epilogue thread
-    static constexpr int NF = P::NF, NS = P::NS, OUT_COLS = P::OUT_COLS;
+    static constexpr int NF = P::NF, NS = P::NS, NB = P::NB, OUT_COLS = P::OUT_COLS;
     static constexpr bool PACKED = P::PACKED;
     static constexpr uint32_t FP32_B_BYTES = BH * BK * 4;
     static constexpr uint32_t FP32_STAGE = FP32_TILE_BYTES + (PACKED ? 0u : FP32_B_BYTES);
     static constexpr uint32_t COMP_A = C::COMP_TILE;                  // one component of op(A)
     static constexpr uint32_t COMP_B = BH * C::ROW_BYTES;             // one component of op(B)
-    static constexpr uint32_t SLICE_STAGE = C::NCOMP * (COMP_A + COMP_B);
+    // component ring stage: op(A)'s components, then op(B)'s (unpacked shapes)
+    static constexpr uint32_t SLICE_STAGE = C::NCOMP * (COMP_A + (PACKED ? 0u : COMP_B));
     static constexpr uint32_t BCOMP_BYTES = C::NCOMP * COMP_B;        // op(B)'s components of a stage
     static constexpr uint32_t IDESC = make_idesc(C::KIND, TILE_M, TN);
     static constexpr uint32_t STAGE_OUT = 32 * OUT_COLS * 4;          // one epilogue warp's staging block
     static constexpr uint32_t SMEM = 1024 /* alignment slack */ + NF * FP32_STAGE + NS * SLICE_STAGE +
-                                     NUM_EPI_WARPS * STAGE_OUT + 1024 /* barriers and flags */;
+                                     NB * BCOMP_BYTES + NUM_EPI_WARPS * STAGE_OUT + 1024 /* barriers and flags */;
     static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
     static_assert(NACC * TN == (int)TMEM_COLS && NACC <= 4, "TMEM accumulators");
 };
@@ -386,7 +389,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 emu_gemm_kernel(const __grid_constant__ Params p) {
     using C = Cfg<MODE>;
     using KC = KCfg<MODE, PIPE>;
-    constexpr int NF = KC::NF, NS = KC::NS, OUT_COLS = KC::OUT_COLS;
+    constexpr int NF = KC::NF, NS = KC::NS, NB = KC::NB, OUT_COLS = KC::OUT_COLS;
     constexpr int TN = KC::TN, BH = KC::BH, NACC = KC::NACC, ACC = KC::ACC;
     constexpr bool PACKED = KC::PACKED;
     constexpr uint32_t STAGE_OUT_BYTES = KC::STAGE_OUT;  // one epilogue warp's 32 x OUT_COLS block
@@ -397,7 +400,8 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t* fp32_ring = smem;
     uint8_t* slice_ring = smem + NF * KC::FP32_STAGE;
-    uint8_t* out_stage = slice_ring + NS * KC::SLICE_STAGE;  // one block per epilogue warp
+    uint8_t* bcomp_ring = slice_ring + NS * KC::SLICE_STAGE;  // packed shapes: op(B)'s components
+    uint8_t* out_stage = bcomp_ring + NB * KC::BCOMP_BYTES;    // one block per epilogue warp
     uint64_t* bars = reinterpret_cast<uint64_t*>(out_stage + NUM_EPI_WARPS * STAGE_OUT_BYTES);
     uint64_t* fp32_full = bars;
     uint64_t* fp32_empty = fp32_full + NF;
@@ -407,7 +411,8 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
     uint64_t* acc_empty = acc_full + NACC;    // leader: both CTAs' epilogue warps
     uint64_t* drain = acc_empty + NACC;
     uint64_t* bcomp_full = drain + 1;          // packed shapes: a stage's op(B) components landed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bcomp_full + NS);
+    uint64_t* bcomp_empty = bcomp_full + NB;   // packed shapes: multicast commit
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bcomp_empty + NB);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
@@ -442,11 +447,11 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
     };
     // packed shapes: op(B)'s component tiles of a stage, straight into the
     // component ring (box {32 k, BH rows, 1 component} per component)
-    auto issue_bload = [&](int ss, int tile, int ks) {
+    auto issue_bload = [&](int bslot, int tile, int ks) {
         const int n0 = (tile % p.tiles_n) * TN + BH * rank;
-        uint64_t* full = &bcomp_full[ss];
+        uint64_t* full = &bcomp_full[bslot];
         mbar_arrive_expect_tx(full, KC::BCOMP_BYTES);
-        uint8_t* dst = slice_ring + ss * KC::SLICE_STAGE + C::NCOMP * KC::COMP_A;
+        uint8_t* dst = bcomp_ring + bslot * KC::BCOMP_BYTES;
         for (int c = 0; c < C::NCOMP; ++c) tma_load_3d(dst + c * KC::COMP_B, &p.tmB, full, ks * BK, n0, c);
     };
     int early = 0, early_b = 0;  // stages already issued by thread 0 (warp 0 lane 0, the producer)
@@ -457,11 +462,11 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         for (int s = 0; s < NS; ++s) { mbar_init(&slice_full[s], 2); mbar_init(&slice_empty[s], 1); }
         for (int b = 0; b < NACC; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 2); }
         mbar_init(drain, 1);
-        for (int s = 0; s < NS; ++s) mbar_init(&bcomp_full[s], 1);
+        for (int s = 0; s < NB; ++s) { mbar_init(&bcomp_full[s], 1); mbar_init(&bcomp_empty[s], 1); }
         *abort_flag = 0;
         fence_mbar_init();
         griddep_wait();
-        const int early_bmax = PACKED ? NS : 0;
+        const int early_bmax = PACKED ? NB : 0;
         for (int u = cid; (early < NF || early_b < early_bmax) && u < p.num_units; u += ncl) {
             const Unit w = unit_of(p, u);
             for (int ks = w.kb; (early < NF || early_b < early_bmax) && ks < w.ke; ++ks) {
@@ -501,13 +506,13 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                     issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
                     if (++s == NF) { s = 0; ph ^= 1u; }
                     if constexpr (PACKED) {
-                        if (n >= early_b) {  // the component slot is free once its MMAs are done
-                            if (!mbar_wait(&slice_empty[bs], bph ^ 1u, abort_flag, budget, 1)) { ok = false; break; }
+                        if (n >= early_b) {  // the slot is free once its stage's MMAs are done
+                            if (!mbar_wait(&bcomp_empty[bs], bph ^ 1u, abort_flag, budget, 1)) { ok = false; break; }
                             issue_bload(bs, w.tile, ks);
                         }
                         bissued_mask |= 1u << bs;
                         bissued_parity = (bissued_parity & ~(1u << bs)) | (bph << bs);
-                        if (++bs == NS) { bs = 0; bph ^= 1u; }
+                        if (++bs == NB) { bs = 0; bph ^= 1u; }
                     }
                 }
             }
@@ -518,7 +523,7 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                         volatile int never = 0;
                         mbar_wait(&fp32_full[t], (issued_parity >> t) & 1u, &never, 50000000ull, 1);
                     }
-                for (int t = 0; t < NS; ++t)
+                for (int t = 0; t < NB; ++t)
                     if (bissued_mask & (1u << t)) {
                         volatile int never = 0;
                         mbar_wait(&bcomp_full[t], (bissued_parity >> t) & 1u, &never, 50000000ull, 1);
@@ -530,10 +535,10 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         // ---------------------------------------------- MMA issuer (leader) -
         setmaxnreg_dec72();
         if (lane == 0 && rank == 0) {
-            int s = 0, b = 0;
+            int s = 0, b = 0, bs = 0;
             uint32_t ph = 0, bph = 0;
             bool ok = true, issued = false;
-            const uint32_t slice_base = smem_u32(slice_ring);
+            const uint32_t slice_base = smem_u32(slice_ring), bcomp_base = smem_u32(bcomp_ring);
             for (int u = cid; ok && u < p.num_units; u += ncl) {
                 const Unit w = unit_of(p, u);
                 for (int ks = w.kb; ks < w.ke; ++ks) {
@@ -541,10 +546,14 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                     if (!mbar_wait(&slice_full[s], ph, abort_flag, budget, 2)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t a_base = slice_base + s * KC::SLICE_STAGE;
-                    const uint32_t b_base = a_base + C::NCOMP * KC::COMP_A;
+                    const uint32_t b_base = PACKED ? bcomp_base + bs * KC::BCOMP_BYTES : a_base + C::NCOMP * KC::COMP_A;
                     issue_stage_mmas<MODE, PIPE>(tmem_base + b * TN, a_base, b_base);
                     issued = true;
                     mma_commit_pair_multicast(&slice_empty[s], 0x3);
+                    if constexpr (PACKED) {
+                        mma_commit_pair_multicast(&bcomp_empty[bs], 0x3);
+                        if (++bs == NB) bs = 0;
+                    }
                     mma_commit_pair_multicast(&acc_full[b], 0x3);
                     if (++s == NS) { s = 0; ph ^= 1u; }
                     if (++b == NACC) { b = 0; bph ^= 1u; }
@@ -562,8 +571,8 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         // ---------------------------------------------------- split warps ---
         setmaxnreg_dec72();
         const uint32_t t = threadIdx.x - WARP_SPLIT0 * 32;
-        int fs = 0, ss = 0;
-        uint32_t fph = 0, sph = 0;
+        int fs = 0, ss = 0, bs = 0;
+        uint32_t fph = 0, sph = 0, bph = 0;
         bool ok = true;
         for (int u = cid; ok && u < p.num_units; u += ncl) {
             const Unit w = unit_of(p, u);
@@ -576,8 +585,9 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                 if constexpr (!PACKED) {
                     split_operand<MODE, NUM_SPLIT_THREADS, BH>(src + FP32_TILE_BYTES, dst + C::NCOMP * KC::COMP_A,
                                                                p.b_mn_major != 0, t);
-                } else {  // op(B)'s components come by TMA into the same slot
-                    if (!mbar_wait_warp(&bcomp_full[ss], sph, abort_flag, budget, 3)) { ok = false; break; }
+                } else {  // op(B)'s components come by TMA into their own ring
+                    if (!mbar_wait_warp(&bcomp_full[bs], bph, abort_flag, budget, 3)) { ok = false; break; }
+                    if (++bs == NB) { bs = 0; bph ^= 1u; }
                 }
                 // one signal per CTA: the split threads meet, then a single
                 // thread releases the stage (a cluster-scope arrive is costly)
