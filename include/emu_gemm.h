@@ -24,10 +24,12 @@
  *   - op(X) = X when the op is EMU_OP_N, X^T when it is EMU_OP_T.
  *   - Pointers: caller-owned DEVICE memory of the current CUDA device.  The
  *     library keeps no caller pointer after the call returns and never frees
- *     caller memory.  Its only device allocation is a split-K workspace
- *     (partial tiles for problems with few tiles), made with cudaMallocAsync
- *     on first need per (device, stream) and kept until the process exits;
- *     emu_sgemm_noalloc never allocates.
+ *     caller memory.  Its only device allocations are a split-K workspace
+ *     (partial tiles for problems with few tiles) and, for the TF32 modes, a
+ *     buffer for op(B) split ahead of the product (when op(A) spans four or
+ *     more 256-row tiles; EMU_AUTOPACK=0 turns that off), made with
+ *     cudaMallocAsync on first need per (device, stream) and kept until the
+ *     process exits; emu_sgemm_noalloc never allocates.
  *   - Alignment (TMA): A and B must start on a 16-byte boundary and lda, ldb
  *     must be multiples of 4 elements; C the same (ldc multiple of 4).
  *     Violations return EMU_STATUS_NOT_SUPPORTED.

@@ -115,3 +115,26 @@ def test_packed_rejects_bad_arguments():
     with pytest.raises(emu.EmuError):
         emu.emu_pack_b(0, 1, 8, 8, B, 8, buf[1:])           # misaligned
     assert emu.emu_pack_bytes(9, 8, 8) == -1
+
+
+@pytest.mark.parametrize("mode", ["tf32x3", "tf32x1"])
+def test_automatic_pre_split_gives_the_same_bits(mode, monkeypatch):
+    """TF32 products with several tile rows split op(B) ahead of the product;
+    the result must not depend on it."""
+    import fp32_emulated_gemm_gb300 as emu
+    rng = np.random.default_rng(33)
+    M, N, K = 1100, 300, 700
+    A = _gpu.to_dev(rng.standard_normal((M, K)).astype(np.float32))
+    B = _gpu.to_dev(rng.standard_normal((K, N)).astype(np.float32))
+    auto = emu.sgemm(A, B, mode=mode).cpu().numpy()
+    monkeypatch.setenv("EMU_AUTOPACK", "0")   # read once per process: use a child process
+    import subprocess, sys, os
+    code = ("import numpy as np, torch, fp32_emulated_gemm_gb300 as emu\n"
+            "rng = np.random.default_rng(33)\n"
+            "A = torch.from_numpy(rng.standard_normal((1100, 700)).astype(np.float32)).cuda()\n"
+            "B = torch.from_numpy(rng.standard_normal((700, 300)).astype(np.float32)).cuda()\n"
+            f"np.save('/tmp/emu_noautopack.npy', emu.sgemm(A, B, mode='{mode}').cpu().numpy())\n")
+    r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ), capture_output=True, text=True,
+                       timeout=300, cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    assert r.returncode == 0, r.stderr[-2000:]
+    _same_bits(auto, np.load("/tmp/emu_noautopack.npy"))
