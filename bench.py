@@ -405,37 +405,80 @@ def load_traffic(args):
 
 
 def run_e2e(emu, mode, s, X, Wt, b, dY, dev, stream, n):
-    """Same step through the public API from pinned host buffers: H2D of the
-    step's inputs, both GEMMs, D2H of both results, every step."""
+    """Same step through the public API from pinned host buffers: every step
+    copies its inputs (X, W, b, dY) host to device, runs both GEMMs and copies
+    both results (Y, dX) device to host.  As an application would, the copies
+    run on their own streams (one per direction) and overlap the GEMMs of the
+    same and the neighbouring steps: the forward waits only for X, W and b,
+    the input gradient for dY, and each result leaves as soon as it is done;
+    device buffers alternate between two sets so that a step's inputs can
+    arrive while the previous step still computes."""
     import torch
     hX, hW, hb, hdY = (torch.from_numpy(a).pin_memory() for a in (X, Wt, b, dY))
-    hY = torch.empty((s.M, s.N)).pin_memory()
-    hdX = torch.empty((s.M, s.K)).pin_memory()
-    Xd, Wd, bd, dYd = (torch.empty_like(t, device=dev) for t in (hX, hW, hb, hdY))
-    Yd = torch.empty((s.M, s.N), device=dev)
-    dXd = torch.empty((s.M, s.K), device=dev)
-    sp = stream.cuda_stream
+    hY = [torch.empty((s.M, s.N)).pin_memory() for _ in range(2)]
+    hdX = [torch.empty((s.M, s.K)).pin_memory() for _ in range(2)]
+    sets = [dict(X=torch.empty_like(hX, device=dev), W=torch.empty_like(hW, device=dev),
+                 b=torch.empty_like(hb, device=dev), dY=torch.empty_like(hdY, device=dev),
+                 Y=torch.empty((s.M, s.N), device=dev), dX=torch.empty((s.M, s.K), device=dev)) for _ in range(2)]
+    h2d = torch.cuda.Stream(dev)
+    d2h = torch.cuda.Stream(dev)
+    comp = stream
+    E = lambda: torch.cuda.Event()
+    freed = [[E(), E()] for _ in range(2)]   # per set: inputs consumed, outputs copied out
+    state = {"i": 0}
 
     def step():
-        for d, h in ((Xd, hX), (Wd, hW), (bd, hb), (dYd, hdY)):
-            d.copy_(h, non_blocking=True)
-        emu.emu_linear_fwd(mode, s.M, s.N, s.K, Xd, Wd, bd, Yd, sp)
-        emu.emu_linear_bwd_input(mode, s.M, s.N, s.K, dYd, Wd, dXd, sp)
-        hY.copy_(Yd, non_blocking=True)
-        hdX.copy_(dXd, non_blocking=True)
+        k = state["i"] % 2
+        d = sets[k]
+        fwd_in, bwd_in, y_done, dx_done = E(), E(), E(), E()
+        with torch.cuda.stream(h2d):
+            h2d.wait_event(freed[k][0])              # the set's previous inputs are consumed
+            d["X"].copy_(hX, non_blocking=True)
+            d["W"].copy_(hW, non_blocking=True)
+            d["b"].copy_(hb, non_blocking=True)
+            fwd_in.record(h2d)
+            d["dY"].copy_(hdY, non_blocking=True)
+            bwd_in.record(h2d)
+        comp.wait_event(fwd_in)
+        comp.wait_event(freed[k][1])                 # the set's previous results have left
+        emu.emu_linear_fwd(mode, s.M, s.N, s.K, d["X"], d["W"], d["b"], d["Y"], comp.cuda_stream)
+        y_done.record(comp)
+        comp.wait_event(bwd_in)
+        emu.emu_linear_bwd_input(mode, s.M, s.N, s.K, d["dY"], d["W"], d["dX"], comp.cuda_stream)
+        dx_done.record(comp)
+        freed[k][0] = E()
+        freed[k][0].record(comp)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(y_done)
+            hY[k].copy_(d["Y"], non_blocking=True)
+            d2h.wait_event(dx_done)
+            hdX[k].copy_(d["dX"], non_blocking=True)
+            freed[k][1] = E()
+            freed[k][1].record(d2h)
+        state["i"] += 1
 
+    for k in range(2):
+        freed[k][0].record(comp)
+        freed[k][1].record(comp)
     for _ in range(3):
         step()
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(comp)
+    h2d.wait_event(e0)
+    d2h.wait_event(e0)
     for _ in range(n):
         step()
-    e1.record(stream)
+    done = [E(), E()]
+    done[0].record(h2d)
+    done[1].record(d2h)
+    comp.wait_event(done[0])
+    comp.wait_event(done[1])
+    e1.record(comp)
     torch.cuda.synchronize(dev)
-    h2d = sum(t.numel() * 4 for t in (hX, hW, hb, hdY))
-    d2h = (hY.numel() + hdX.numel()) * 4
-    return {"ms": e0.elapsed_time(e1) / n, "h2d": h2d, "d2h": d2h}
+    h2d_bytes = sum(t.numel() * 4 for t in (hX, hW, hb, hdY))
+    d2h_bytes = (hY[0].numel() + hdX[0].numel()) * 4
+    return {"ms": e0.elapsed_time(e1) / n, "h2d": h2d_bytes, "d2h": d2h_bytes}
 
 
 if __name__ == "__main__":
