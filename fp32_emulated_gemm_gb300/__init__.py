@@ -18,10 +18,12 @@ import os
 import threading
 
 __all__ = [
-    "EMU_MODE_BF16X9", "EMU_MODE_TF32X3", "EMU_MODE_TF32X1", "EMU_MODE_BF16X6", "EMU_OP_N", "EMU_OP_T",
+    "EMU_MODE_BF16X9", "EMU_MODE_TF32X3", "EMU_MODE_TF32X1", "EMU_MODE_BF16X6", "EMU_MODE_FP32", "EMU_OP_N",
+    "EMU_OP_T", "EMU_STRATEGY_EAGER", "EMU_STRATEGY_PERFORMANT",
     "EmuError",
     "emu_sgemm", "emu_linear_fwd", "emu_linear_bwd_input", "emu_linear_bwd_weight", "emu_status_string",
     "emu_stream_check", "emu_split_dump", "emu_plan_query", "emu_version",
+    "emu_set_strategy", "emu_get_strategy", "emu_dispatch_query", "strategy",
     "emu_pack_bytes", "emu_pack_b", "emu_sgemm_packed_b", "emu_linear_fwd_packed", "emu_linear_bwd_input_packed",
     "pack_b", "sgemm_packed", "PackedWeight", "pack_weight", "linear_fwd_packed", "linear_bwd_input_packed",
     "sgemm", "linear_fwd", "linear_bwd_input", "linear_bwd_weight", "EmuLinearFunction", "EmuLinear",
@@ -32,10 +34,14 @@ EMU_MODE_BF16X9 = 0
 EMU_MODE_TF32X3 = 1
 EMU_MODE_TF32X1 = 2
 EMU_MODE_BF16X6 = 3
+EMU_MODE_FP32 = 4
 EMU_OP_N = 0
 EMU_OP_T = 1
+EMU_STRATEGY_EAGER = 0
+EMU_STRATEGY_PERFORMANT = 1
 MODES = {"bf16x9": EMU_MODE_BF16X9, "tf32x3": EMU_MODE_TF32X3, "tf32x1": EMU_MODE_TF32X1,
-         "bf16x6": EMU_MODE_BF16X6}
+         "bf16x6": EMU_MODE_BF16X6, "fp32": EMU_MODE_FP32}
+STRATEGIES = {"eager": EMU_STRATEGY_EAGER, "performant": EMU_STRATEGY_PERFORMANT}
 
 STATUS_NAMES = {
     0: "EMU_STATUS_SUCCESS", 1: "EMU_STATUS_INVALID_VALUE", 2: "EMU_STATUS_NOT_SUPPORTED",
@@ -89,6 +95,12 @@ def load():
         L.emu_plan_query.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64), i32]
         L.emu_plan_query.restype = i32
         L.emu_version.argtypes = []
+        L.emu_set_strategy.argtypes = [i32]
+        L.emu_set_strategy.restype = i32
+        L.emu_get_strategy.argtypes = []
+        L.emu_get_strategy.restype = i32
+        L.emu_dispatch_query.argtypes = [i32, i64, i64, i64, i32, ctypes.POINTER(i32)]
+        L.emu_dispatch_query.restype = i32
         for name in ("emu_sgemm", "emu_linear_fwd", "emu_linear_bwd_input", "emu_linear_bwd_weight",
                      "emu_stream_check",
                      "emu_split_dump", "emu_version"):
@@ -149,7 +161,7 @@ def emu_split_dump(mode, R, Kc, X, ldx, mn_major, out, stream=None):
 
 
 def emu_pack_bytes(mode, N, K) -> int:
-    return int(load().emu_pack_bytes(int(mode), int(N), int(K)))
+    return int(load().emu_pack_bytes(_mode(mode), int(N), int(K)))
 
 
 def emu_pack_b(mode, transB, N, K, B, ldb, packed, stream=None):
@@ -175,7 +187,7 @@ def emu_linear_bwd_input_packed(mode, M, N, K, dY, Wt_packed, dX, stream=None):
 
 
 PLAN_FIELDS = ("pipe", "tile_n", "tiles_m", "tiles_n", "k_stages", "tiles_a", "split_a", "split_b",
-               "units", "pairs", "slots")
+               "units", "pairs", "slots", "cost_x100")
 
 
 def emu_plan_query(M, N, K, pairs) -> dict:
@@ -187,6 +199,46 @@ def emu_plan_query(M, N, K, pairs) -> dict:
 
 def emu_version() -> int:
     return int(load().emu_version())
+
+
+def emu_set_strategy(strategy) -> None:
+    """Process-wide strategy: "eager" (always the requested mode) or
+    "performant" (native FP32 where emulation is predicted slower)."""
+    s = STRATEGIES[strategy] if isinstance(strategy, str) else int(strategy)
+    _check(load().emu_set_strategy(s), "emu_set_strategy")
+
+
+def emu_get_strategy() -> str:
+    v = int(load().emu_get_strategy())
+    return {c: n for n, c in STRATEGIES.items()}[v]
+
+
+def emu_dispatch_query(mode, M, N, K, pairs=76) -> str:
+    """The mode emu_sgemm would run an M x N x K product in under the current
+    strategy (host only)."""
+    out = ctypes.c_int(-1)
+    _check(load().emu_dispatch_query(_mode(mode), int(M), int(N), int(K), int(pairs), ctypes.byref(out)),
+           "emu_dispatch_query")
+    return {c: n for n, c in MODES.items()}[out.value]
+
+
+class strategy:
+    """Context manager: run the enclosed calls under another strategy, then
+    restore the previous one (process-wide, so not for concurrent threads
+    that want different strategies)."""
+
+    def __init__(self, name):
+        self.name = name
+        self.prev = None
+
+    def __enter__(self):
+        self.prev = emu_get_strategy()
+        emu_set_strategy(self.name)
+        return self
+
+    def __exit__(self, *exc):
+        emu_set_strategy(self.prev)
+        return False
 
 
 # ----------------------------------------------------- tensor helpers ------

@@ -14,6 +14,8 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <atomic>
+#include <cmath>
 #include <mutex>
 
 #include "../../include/emu_gemm.h"
@@ -68,10 +70,12 @@ cudaError_t set_smem_attr() {
                                 smem_bytes<MODE, PIPE>());
 }
 
-bool valid_mode(emu_mode_t mode) {
+// the emulated modes (tensor cores); EMU_MODE_FP32 is the native one
+bool emulated_mode(emu_mode_t mode) {
     return mode == EMU_MODE_BF16X9 || mode == EMU_MODE_TF32X3 || mode == EMU_MODE_TF32X1 ||
            mode == EMU_MODE_BF16X6;
 }
+bool valid_mode(emu_mode_t mode) { return emulated_mode(mode) || mode == EMU_MODE_FP32; }
 
 const char* mode_name(emu_mode_t mode) {
     switch (mode) {
@@ -79,6 +83,7 @@ const char* mode_name(emu_mode_t mode) {
         case EMU_MODE_TF32X3: return "tf32x3";
         case EMU_MODE_TF32X1: return "tf32x1";
         case EMU_MODE_BF16X6: return "bf16x6";
+        case EMU_MODE_FP32: return "fp32";
     }
     return "?";
 }
@@ -262,6 +267,155 @@ __global__ void pack_kernel(int64_t rows, int64_t K, const float* B, int64_t ldb
     }
 }
 
+// ---------------------------------------------------------- native FP32 ----
+// C = alpha op(A) op(B) + beta C_old + bias on the CUDA cores: each output is
+// one chain acc = fmaf(a_k, b_k, acc) over k = 0, 1, ..., K-1 from acc = +0,
+// then C = fmaf(alpha, acc, beta * C_old) (beta == 0: C_old not read), plus
+// the bias when there is one.  A block of 16 x 16 threads computes a 16R x 16R
+// tile of C, R x R outputs per thread (rows R ty + i, columns R tx + j), from
+// 16-deep k-slices of op(A) and op(B) staged in shared memory.  The chains
+// cannot be split along k, so small outputs take a smaller R to occupy the SMs.
+constexpr int NAT_KT = 16, NAT_MAX_GRID_Y = 65535;
+template <int R>
+__global__ void __launch_bounds__(256) native_sgemm_kernel(int M, int N, int K, float alpha, const float* A,
+                                                           long long lda, int a_mn, const float* B, long long ldb,
+                                                           int b_mn, float beta, float* C, long long ldc,
+                                                           const float* bias) {
+    constexpr int T = 16 * R, LD = T + 4;  // +4: fewer bank conflicts, rows stay 16-byte aligned
+    __shared__ __align__(16) float As[NAT_KT][LD];
+    __shared__ __align__(16) float Bs[NAT_KT][LD];
+    const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+    const int m0 = blockIdx.x * T, n0 = blockIdx.y * T;
+    float acc[R][R];
+#pragma unroll
+    for (int i = 0; i < R; ++i)
+#pragma unroll
+        for (int j = 0; j < R; ++j) acc[i][j] = 0.0f;
+    // each slice is 16 x T elements, R per thread: element e = threadIdx.x + 256 q
+    // is (k, r) = (e / T, e % T) for an MN-major source and (e % 16, e / 16)
+    // for a K-major one, so that neighbouring threads read neighbouring
+    // addresses.  The next slice is fetched into registers while the current
+    // one is used.
+    float ra_[R], rb_[R];
+    auto fetch = [&](int k0) {
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const int e = threadIdx.x + 256 * q;
+            const int ka = a_mn ? e / T : e % 16, ra = a_mn ? e % T : e / 16;
+            const int gm = m0 + ra, gka = k0 + ka;
+            ra_[q] = (gm < M && gka < K) ? A[a_mn ? (long long)gka * lda + gm : (long long)gm * lda + gka] : 0.0f;
+            const int kb = b_mn ? e / T : e % 16, cb = b_mn ? e % T : e / 16;
+            const int gn = n0 + cb, gkb = k0 + kb;
+            rb_[q] = (gn < N && gkb < K) ? B[b_mn ? (long long)gkb * ldb + gn : (long long)gn * ldb + gkb] : 0.0f;
+        }
+    };
+    auto step = [&](int k) {
+        float av[R], bv[R];
+        if constexpr (R == 4) {
+            const float4 a = *reinterpret_cast<const float4*>(&As[k][4 * ty]);
+            const float4 b = *reinterpret_cast<const float4*>(&Bs[k][4 * tx]);
+            av[0] = a.x; av[1] = a.y; av[2] = a.z; av[3] = a.w;
+            bv[0] = b.x; bv[1] = b.y; bv[2] = b.z; bv[3] = b.w;
+        } else if constexpr (R == 2) {
+            const float2 a = *reinterpret_cast<const float2*>(&As[k][2 * ty]);
+            const float2 b = *reinterpret_cast<const float2*>(&Bs[k][2 * tx]);
+            av[0] = a.x; av[1] = a.y;
+            bv[0] = b.x; bv[1] = b.y;
+        } else {
+            av[0] = As[k][ty];
+            bv[0] = Bs[k][tx];
+        }
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+            for (int j = 0; j < R; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
+    };
+    if (K > 0) fetch(0);
+    for (int k0 = 0; k0 < K; k0 += NAT_KT) {
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const int e = threadIdx.x + 256 * q;
+            As[a_mn ? e / T : e % 16][a_mn ? e % T : e / 16] = ra_[q];
+            Bs[b_mn ? e / T : e % 16][b_mn ? e % T : e / 16] = rb_[q];
+        }
+        __syncthreads();
+        if (k0 + NAT_KT < K) fetch(k0 + NAT_KT);
+        if (K - k0 >= NAT_KT) {
+#pragma unroll
+            for (int k = 0; k < NAT_KT; ++k) step(k);
+        } else {
+            for (int k = 0; k < K - k0; ++k) step(k);  // only k < K enters the chains
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+        const int gm = m0 + R * ty + i;
+        if (gm >= M) continue;
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const int gn = n0 + R * tx + j;
+            if (gn >= N) continue;
+            float* c = C + (long long)gm * ldc + gn;
+            const float bc = beta != 0.0f ? __fmul_rn(beta, *c) : 0.0f;
+            float v = __fmaf_rn(alpha, acc[i][j], bc);
+            if (bias) v = __fadd_rn(v, bias[gn]);
+            *c = v;
+        }
+    }
+}
+
+// The largest R whose grid still gives every SM a block.
+int native_r(int64_t M, int64_t N, int sm_count) {
+    for (int R = 4; R > 1; R /= 2) {
+        const int64_t t = 16 * R, blocks = ((M + t - 1) / t) * ((N + t - 1) / t);
+        if (blocks >= sm_count && (N + t - 1) / t <= NAT_MAX_GRID_Y) return R;
+    }
+    return 1;
+}
+
+cudaError_t launch_native(int64_t M, int64_t N, int64_t K, float alpha, const float* A, int64_t lda, bool a_mn,
+                          const float* B, int64_t ldb, bool b_mn, float beta, float* C, int64_t ldc,
+                          const float* bias, int sm_count, cudaStream_t stream) {
+    int R = native_r(M, N, sm_count);
+    while (R < 4 && (N + 16 * R - 1) / (16 * R) > NAT_MAX_GRID_Y) R *= 2;
+    const int64_t t = 16 * R, gx = (M + t - 1) / t, gy = (N + t - 1) / t;
+    if (gy > NAT_MAX_GRID_Y || gx > INT32_MAX) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)gx, (unsigned)gy, 1);
+    cudaGetLastError();
+    switch (R) {
+        case 4: native_sgemm_kernel<4><<<grid, 256, 0, stream>>>((int)M, (int)N, (int)K, alpha, A, lda, a_mn, B, ldb,
+                                                                 b_mn, beta, C, ldc, bias); break;
+        case 2: native_sgemm_kernel<2><<<grid, 256, 0, stream>>>((int)M, (int)N, (int)K, alpha, A, lda, a_mn, B, ldb,
+                                                                 b_mn, beta, C, ldc, bias); break;
+        default: native_sgemm_kernel<1><<<grid, 256, 0, stream>>>((int)M, (int)N, (int)K, alpha, A, lda, a_mn, B,
+                                                                  ldb, b_mn, beta, C, ldc, bias);
+    }
+    return cudaGetLastError();
+}
+
+std::atomic<int> g_strategy{EMU_STRATEGY_EAGER};
+
+// Predicted GPU times in microseconds on GB300, fitted to measured kernel
+// times (CUDA graphs of back-to-back calls, 66 shapes from 64^3 to 2048^3,
+// rms error about 6% emulated and 12% native).  Emulated: a fixed start-up,
+// the plan's pipeline stages (waves x (k-stages + stores)) at the mode's
+// stage time, and for split tiles a reduction that grows with the pieces per
+// tile.  Native: a fixed cost plus one step per 16-deep k-slice, whose time
+// grows with the FMAs each SM carries per slice.
+struct EmuTimeModel { double fixed, stage, split_fixed, split_per_piece; };
+EmuTimeModel emu_time_model(emu_mode_t mode) {
+    switch (mode) {
+        case EMU_MODE_BF16X9: return {3.8, 1.262, 2.64, 0.51};
+        case EMU_MODE_TF32X3: return {3.9, 1.572, 2.96, 0.44};
+        // the comparators were not fitted: BF16x9's start-up and reduction,
+        // stage times estimated from their share of the MMA work
+        case EMU_MODE_BF16X6: return {3.8, 1.0, 2.64, 0.51};
+        default: return {3.8, 0.8, 2.64, 0.51};  // TF32x1
+    }
+}
+constexpr double kNatFixedUs = 1.6, kNatSliceUs = 0.342, kNatSlicePerSmFmaUs = 0.0479 / (256.0 * 16.0);
+
 __global__ void scale_kernel(int64_t M, int64_t N, float beta, float* C, int64_t ldc, const float* bias) {
     const int64_t total = M * N;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -364,6 +518,7 @@ struct Plan {
     int num_units;
     int clusters;   // CTA pairs launched
     long long slots;  // workspace partial tiles (0: no split tile)
+    double cost;      // predicted time in pipeline stages (see below)
 };
 
 // Long k-loops per work unit favour three component stages; short ones the
@@ -416,7 +571,9 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int pairs) {
     const int s_max = KS < 32 ? KS : 32;
     if (force_split >= 1) {
         int S = force_split < s_max ? force_split : s_max;
-        set_uniform(S < pairs ? S : pairs);
+        S = S < pairs ? S : pairs;
+        set_uniform(S);
+        plan.cost = cost_uniform(S);
     } else {
         double best = -1.0;
         for (int S = 1; S <= s_max && S <= pairs; ++S) {
@@ -436,6 +593,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int pairs) {
                 }
             }
         }
+        plan.cost = best;
     }
     plan.num_units = plan.tiles_a * plan.split_a + (plan.num_tiles - plan.tiles_a) * plan.split_b;
     plan.slots = (plan.split_a > 1 ? (long long)plan.tiles_a * plan.split_a : 0) +
@@ -445,6 +603,23 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int pairs) {
     plan.pipe = force_pipe == PIPE_SHORT_K || force_pipe == PIPE_LONG_K ? force_pipe
               : per_unit >= kLongKMinStages ? PIPE_LONG_K : PIPE_SHORT_K;
     return plan;
+}
+
+// The mode a product runs in: the requested one, except that the performant
+// strategy runs an emulated product in native FP32 when that is predicted
+// faster.  `pairs`: the device's co-resident CTA pairs; `sm_count`: its SMs.
+emu_mode_t dispatch_mode(emu_mode_t mode, int64_t M, int64_t N, int64_t K, int pairs, int sm_count) {
+    if (mode == EMU_MODE_FP32 || g_strategy.load(std::memory_order_relaxed) != EMU_STRATEGY_PERFORMANT) return mode;
+    const Plan plan = make_plan(M, N, K, pairs);
+    const int S = plan.split_a > plan.split_b ? plan.split_a : plan.split_b;
+    const EmuTimeModel em = emu_time_model(mode);
+    const double emu_us = em.fixed + em.stage * (plan.cost - (S > 1 ? kReduceStages : 0.0)) +
+                          (S > 1 ? em.split_fixed + em.split_per_piece * S : 0.0);
+    const int R = native_r(M, N, sm_count);
+    const double t = 16.0 * R, blocks = std::ceil((double)M / t) * std::ceil((double)N / t);
+    const double fma_per_sm = blocks / sm_count * 256.0 * 16.0 * R * R;
+    const double nat_us = kNatFixedUs + std::ceil((double)K / NAT_KT) * (kNatSliceUs + kNatSlicePerSmFmaUs * fma_per_sm);
+    return nat_us < emu_us ? EMU_MODE_FP32 : mode;
 }
 
 unsigned long long wait_budget_ns() {
@@ -565,6 +740,15 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
     }
 
     const int pairs = dev->max_clusters[mode == EMU_MODE_TF32X3 ? 1 : 0];
+    if (!packed_b) mode = dispatch_mode(mode, M, N, K, pairs, dev->sm_count);
+    if (mode == EMU_MODE_FP32) {
+        if (N > 64LL * NAT_MAX_GRID_Y) return EMU_STATUS_NOT_SUPPORTED;
+        if (log_enabled())
+            std::fprintf(stderr, "[emu] fp32 M=%lld N=%lld K=%lld a_mn=%d b_mn=%d (native)\n", (long long)M,
+                         (long long)N, (long long)K, (int)a_mn, (int)b_mn);
+        return launch_native(M, N, K, alpha, A, lda, a_mn, B, ldb, b_mn, beta, C, ldc, bias, dev->sm_count, stream) == cudaSuccess
+                   ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
+    }
     Plan plan = make_plan(M, N, K, pairs);
     static const bool autopack = env_int("EMU_AUTOPACK", 1) != 0;
     if (!packed_b && autopack && (mode == EMU_MODE_TF32X3 || mode == EMU_MODE_TF32X1) &&
@@ -618,8 +802,7 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
 }
 
 // ----------------------------------------------------------- split dump ----
-// One tile of ROWS rows (128: the op(A) tile; 64: the op(B) tile of TN = 128
-// plans) through the kernel's split.
+// One 128-row operand tile through the kernel's split.
 template <int MODE, int ROWS>
 __global__ void __launch_bounds__(256, 1) split_dump_kernel(const __grid_constant__ CUtensorMap tm, int R, int Kc,
                                                             int mn_major, void* out) {
@@ -716,13 +899,13 @@ emu_status_t emu_linear_bwd_weight(emu_mode_t mode, int64_t M, int64_t N, int64_
 }
 
 int64_t emu_pack_bytes(emu_mode_t mode, int64_t N, int64_t K) {
-    if (!valid_mode(mode) || N < 0 || K < 0) return -1;
+    if (!emulated_mode(mode) || N < 0 || K < 0) return -1;
     return packed_bytes(mode, N, K);
 }
 
 emu_status_t emu_pack_b(emu_mode_t mode, emu_op_t transB, int64_t N, int64_t K, const float* B, int64_t ldb,
                         void* packed, emu_stream_t stream) {
-    if (!valid_mode(mode) || (transB != EMU_OP_N && transB != EMU_OP_T)) return EMU_STATUS_INVALID_VALUE;
+    if (!emulated_mode(mode) || (transB != EMU_OP_N && transB != EMU_OP_T)) return EMU_STATUS_INVALID_VALUE;
     if (N < 0 || K < 0) return EMU_STATUS_INVALID_VALUE;
     if (N > INT32_MAX - 256 || K > INT32_MAX - 256) return EMU_STATUS_NOT_SUPPORTED;
     if (N == 0 || K == 0) return EMU_STATUS_SUCCESS;
@@ -739,7 +922,7 @@ emu_status_t emu_pack_b(emu_mode_t mode, emu_op_t transB, int64_t N, int64_t K, 
 emu_status_t emu_sgemm_packed_b(emu_mode_t mode, emu_op_t transA, int64_t M, int64_t N, int64_t K, float alpha,
                                 const float* A, int64_t lda, const void* packed_b, float beta, float* C,
                                 int64_t ldc, emu_stream_t stream) {
-    if (transA != EMU_OP_N && transA != EMU_OP_T) return EMU_STATUS_INVALID_VALUE;
+    if (!emulated_mode(mode) || (transA != EMU_OP_N && transA != EMU_OP_T)) return EMU_STATUS_INVALID_VALUE;
     if (!packed_b && K > 0 && alpha != 0.0f) return EMU_STATUS_INVALID_VALUE;
     return run_gemm(mode, transA == EMU_OP_T, false, M, N, K, alpha, A, lda, nullptr, 0, beta, C, ldc, nullptr,
                     reinterpret_cast<cudaStream_t>(stream), packed_b);
@@ -747,14 +930,14 @@ emu_status_t emu_sgemm_packed_b(emu_mode_t mode, emu_op_t transA, int64_t M, int
 
 emu_status_t emu_linear_fwd_packed(emu_mode_t mode, int64_t M, int64_t N, int64_t K, const float* X,
                                    const void* W_packed, const float* bias, float* Y, emu_stream_t stream) {
-    if (!W_packed && K > 0) return EMU_STATUS_INVALID_VALUE;
+    if (!emulated_mode(mode) || (!W_packed && K > 0)) return EMU_STATUS_INVALID_VALUE;
     return run_gemm(mode, false, false, M, N, K, 1.0f, X, K, nullptr, 0, 0.0f, Y, N, bias,
                     reinterpret_cast<cudaStream_t>(stream), W_packed);
 }
 
 emu_status_t emu_linear_bwd_input_packed(emu_mode_t mode, int64_t M, int64_t N, int64_t K, const float* dY,
                                          const void* Wt_packed, float* dX, emu_stream_t stream) {
-    if (!Wt_packed && N > 0) return EMU_STATUS_INVALID_VALUE;
+    if (!emulated_mode(mode) || (!Wt_packed && N > 0)) return EMU_STATUS_INVALID_VALUE;
     return run_gemm(mode, false, false, M, K, N, 1.0f, dY, N, nullptr, 0, 0.0f, dX, K, nullptr,
                     reinterpret_cast<cudaStream_t>(stream), Wt_packed);
 }
@@ -789,14 +972,12 @@ emu_status_t emu_split_dump(emu_mode_t mode, int64_t R, int64_t Kc, const float*
     DeviceInfo* dev = nullptr;
     emu_status_t st = device_info(&dev);
     if (st != EMU_STATUS_SUCCESS) return st;
-    const bool rows64 = R <= 64;
     CUtensorMap tm;
-    if (!encode_operand(&tm, X, mn_major != 0, R, Kc, ldx, rows64 ? 64u : (uint32_t)HALF))
-        return EMU_STATUS_LAUNCH_FAILED;
+    if (!encode_operand(&tm, X, mn_major != 0, R, Kc, ldx, (uint32_t)HALF)) return EMU_STATUS_LAUNCH_FAILED;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int R32 = (int)R, K32 = (int)Kc;
     // shared memory: FP32 tile, the components, the barrier, alignment slack
-    const uint32_t rows = rows64 ? 64u : (uint32_t)HALF;
+    const uint32_t rows = HALF;
     const uint32_t bytes = mode == EMU_MODE_BF16X9
         ? 1024 + rows * BK * 4 + 3 * rows * Cfg<MODE_BF16X9>::ROW_BYTES + 64
         : 1024 + rows * BK * 4 + 2 * rows * Cfg<MODE_TF32X3>::ROW_BYTES + 64;
@@ -805,13 +986,8 @@ emu_status_t emu_split_dump(emu_mode_t mode, int64_t R, int64_t Kc, const float*
         cudaGetLastError();
         kernel<<<1, 256, bytes, s>>>(tm, R32, K32, mn_major, out);
     };
-    if (mode == EMU_MODE_BF16X9) {
-        if (rows64) run(split_dump_kernel<MODE_BF16X9, 64>);
-        else run(split_dump_kernel<MODE_BF16X9, HALF>);
-    } else {
-        if (rows64) run(split_dump_kernel<MODE_TF32X3, 64>);
-        else run(split_dump_kernel<MODE_TF32X3, HALF>);
-    }
+    if (mode == EMU_MODE_BF16X9) run(split_dump_kernel<MODE_BF16X9, HALF>);
+    else run(split_dump_kernel<MODE_TF32X3, HALF>);
     return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
 }
 
@@ -830,8 +1006,24 @@ emu_status_t emu_plan_query(int64_t M, int64_t N, int64_t K, int pairs, int64_t*
     if (M > INT32_MAX - 256 || N > INT32_MAX - 256 || K > INT32_MAX - 256) return EMU_STATUS_NOT_SUPPORTED;
     const Plan p = make_plan(M, N, K, pairs);
     const int64_t v[EMU_PLAN_FIELDS] = {p.pipe, p.tn, p.tiles_m, p.tiles_n, p.k_stages, p.tiles_a,
-                                        p.split_a, p.split_b, p.num_units, p.clusters, p.slots};
+                                        p.split_a, p.split_b, p.num_units, p.clusters, p.slots,
+                                        (int64_t)(p.cost * 100.0 + 0.5)};
     for (int i = 0; i < EMU_PLAN_FIELDS; ++i) out[i] = v[i];
+    return EMU_STATUS_SUCCESS;
+}
+
+emu_status_t emu_set_strategy(emu_strategy_t strategy) {
+    if (strategy != EMU_STRATEGY_EAGER && strategy != EMU_STRATEGY_PERFORMANT) return EMU_STATUS_INVALID_VALUE;
+    g_strategy.store(strategy, std::memory_order_relaxed);
+    return EMU_STATUS_SUCCESS;
+}
+
+emu_strategy_t emu_get_strategy(void) { return static_cast<emu_strategy_t>(g_strategy.load(std::memory_order_relaxed)); }
+
+emu_status_t emu_dispatch_query(emu_mode_t mode, int64_t M, int64_t N, int64_t K, int pairs, emu_mode_t* out) {
+    if (!valid_mode(mode) || M <= 0 || N <= 0 || K <= 0 || pairs < 1 || !out) return EMU_STATUS_INVALID_VALUE;
+    if (M > INT32_MAX - 256 || N > INT32_MAX - 256 || K > INT32_MAX - 256) return EMU_STATUS_NOT_SUPPORTED;
+    *out = dispatch_mode(mode, M, N, K, pairs, 2 * pairs);
     return EMU_STATUS_SUCCESS;
 }
 
@@ -913,6 +1105,11 @@ emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, 
     }
 
     const int pairs = dev->max_clusters[mode == EMU_MODE_TF32X3 ? 1 : 0];
+    if (dispatch_mode(mode, M, N, K, pairs, dev->sm_count) == EMU_MODE_FP32) {
+        if (N > 64LL * NAT_MAX_GRID_Y) return EMU_STATUS_NOT_SUPPORTED;
+        return launch_native(M, N, K, alpha, A, lda, a_mn, B, ldb, b_mn, beta, C, ldc, nullptr, dev->sm_count, stream) == cudaSuccess
+                   ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
+    }
     const Plan plan = make_plan(M, N, K, pairs);
     Params p{};
     if (!encode_operand(&p.tmA, A, a_mn, M, K, lda, HALF) ||

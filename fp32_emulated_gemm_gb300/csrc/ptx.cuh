@@ -271,6 +271,10 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  ::"r"(smem_u32(bar)) : "memory");
 }
+// Per-warpgroup register budgets.  The CTA launches 512 threads with 128
+// registers each (65,536); the two warpgroups of producer, MMA and split
+// warps give up 56 each and the two epilogue warpgroups take 56 more each:
+// 2 x 128 x 72 + 2 x 128 x 184 = 65,536, so the increase never waits.
 __device__ __forceinline__ void setmaxnreg_dec72() { asm volatile("setmaxnreg.dec.sync.aligned.u32 72;" ::: "memory"); }
 __device__ __forceinline__ void setmaxnreg_inc184() { asm volatile("setmaxnreg.inc.sync.aligned.u32 184;" ::: "memory"); }
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {

@@ -71,7 +71,11 @@ typedef enum {
     EMU_MODE_TF32X1 = 2, /* one-pass TF32: hi(a) hi(b) only ("TF32x3 on Ampere GPUs": the one-pass
                             mode whose force jitter and drift the blog reports); error up to
                             2^-10 |a||b| per product */
-    EMU_MODE_BF16X6 = 3  /* BF16x9 without bands 3 and 4 (six products); error up to 2^-20 |a||b| */
+    EMU_MODE_BF16X6 = 3, /* BF16x9 without bands 3 and 4 (six products); error up to 2^-20 |a||b| */
+    /* Native FP32, the performant strategy's choice for small products: */
+    EMU_MODE_FP32 = 4    /* CUDA cores, no tensor cores: each output is one chain of fmaf over
+                            k = 0, 1, ..., K-1 from +0, then the epilogue.  No packed form;
+                            N above 4,194,240 is NOT_SUPPORTED. */
 } emu_mode_t;
 
 typedef enum { EMU_OP_N = 0, EMU_OP_T = 1 } emu_op_t;
@@ -143,14 +147,15 @@ emu_status_t emu_linear_bwd_weight(emu_mode_t mode, int64_t M, int64_t N, int64_
  * the operand is split into the mode's components once, and later products
  * load the components directly (no per-call split of that operand, fewer
  * shared-memory bytes per k-stage).  Results are the same bits as the
- * unpacked calls.  The blog describes the cuBLAS "performant" strategy
- * ("BF16x9 on Blackwell GPUs"); splitting a fixed weight once is this
- * library's form of saving per-call work.
+ * unpacked calls.  Splitting a fixed weight once saves per-call work
+ * where the blog's performant strategy ("BF16x9 on Blackwell GPUs") saves
+ * it by choosing native FP32 (see emu_set_strategy).
  *
  * emu_pack_bytes -- device bytes a packed op(B) of N x K (output width N,
  *   contraction K) takes in `mode`: ncomp * N * Kp * elem, Kp = K rounded up
  *   to 32, elem 2 (BF16 modes) or 4 (TF32 modes), ncomp 3 / 2 / 1.  -1 for an
- *   invalid mode or negative size.
+ *   invalid mode, EMU_MODE_FP32 or a negative size.  The packing calls return
+ *   INVALID_VALUE for EMU_MODE_FP32.
  * emu_pack_b -- write the packed form of op(B) (K x N; transB as in
  *   emu_sgemm, B row-major with leading dimension ldb, device memory) to
  *   `packed` (device memory, emu_pack_bytes bytes, 16-byte aligned,
@@ -266,13 +271,41 @@ emu_status_t emu_selftest_wait_timeout(uint64_t budget_ns, emu_stream_t stream);
  *   6 pieces per tile of those (split_a)     7 pieces per remaining tile (split_b)
  *   8 work units                             9 CTA pairs launched
  *  10 workspace partial tiles (256 x 256 FP32 each; 0 = no split tile)
+ *  11 predicted time in hundredths of a pipeline stage (waves of work
+ *     units, each its k-stages plus the output stores, plus the split-K
+ *     reduction), the figure the plan minimises
  * Work unit u of the first group is piece u % split_a of tile u / split_a;
  * the remaining tiles follow, split_b units each; pair c runs units c,
  * c + pairs launched, ...  INVALID_VALUE for non-positive sizes, pairs < 1,
  * a NULL `out` or n < EMU_PLAN_FIELDS.
  */
-#define EMU_PLAN_FIELDS 11
+#define EMU_PLAN_FIELDS 12
 emu_status_t emu_plan_query(int64_t M, int64_t N, int64_t K, int pairs, int64_t *out, int n);
+
+/*
+ * Strategy.  Blog: "BF16x9 on Blackwell GPUs" (Fig. 4) compares two: the
+ * eager one emulates whenever the operation allows it, the performant one
+ * only where emulation is expected to beat native FP32.
+ *   EMU_STRATEGY_EAGER (default): every product runs in the requested mode.
+ *   EMU_STRATEGY_PERFORMANT: emu_sgemm, the unpacked emu_linear_* calls and
+ *     emu_sgemm_noalloc
+ *     run a product whose emulated form is predicted slower in
+ *     EMU_MODE_FP32 instead (on GB300: small products, below about
+ *     0.5 GFLOP).  Packed-operand calls always emulate.
+ * Process-wide; emu_set_strategy returns INVALID_VALUE for an unknown value.
+ */
+typedef enum { EMU_STRATEGY_EAGER = 0, EMU_STRATEGY_PERFORMANT = 1 } emu_strategy_t;
+emu_status_t emu_set_strategy(emu_strategy_t strategy);
+emu_strategy_t emu_get_strategy(void);
+
+/*
+ * emu_dispatch_query -- host only (no GPU, no CUDA call): the mode in which
+ * emu_sgemm would run an M x N x K product requested in `mode` under the
+ * current strategy, on a device with `pairs` co-resident CTA pairs and
+ * 2 * pairs SMs (76 pairs on a GB300).  INVALID_VALUE for an unknown mode,
+ * non-positive sizes, pairs < 1 or a NULL `out`.
+ */
+emu_status_t emu_dispatch_query(emu_mode_t mode, int64_t M, int64_t N, int64_t K, int pairs, emu_mode_t *out);
 
 /* Library version as an integer (major * 10000 + minor * 100 + patch). */
 int emu_version(void);

@@ -47,10 +47,15 @@ def test_library_exports_every_declared_symbol(lib):
 def test_enums_match_binding():
     modes = _declared_enum("EMU_MODE_")
     assert modes == {"EMU_MODE_BF16X9": emu.EMU_MODE_BF16X9, "EMU_MODE_TF32X3": emu.EMU_MODE_TF32X3,
-                     "EMU_MODE_TF32X1": emu.EMU_MODE_TF32X1, "EMU_MODE_BF16X6": emu.EMU_MODE_BF16X6}
+                     "EMU_MODE_TF32X1": emu.EMU_MODE_TF32X1, "EMU_MODE_BF16X6": emu.EMU_MODE_BF16X6,
+                     "EMU_MODE_FP32": emu.EMU_MODE_FP32}
     assert {f"EMU_MODE_{k.upper()}": v for k, v in emu.MODES.items()} == modes
     ops = _declared_enum("EMU_OP_")
     assert ops == {"EMU_OP_N": emu.EMU_OP_N, "EMU_OP_T": emu.EMU_OP_T}
+    strategies = _declared_enum("EMU_STRATEGY_")
+    assert strategies == {"EMU_STRATEGY_EAGER": emu.EMU_STRATEGY_EAGER,
+                          "EMU_STRATEGY_PERFORMANT": emu.EMU_STRATEGY_PERFORMANT}
+    assert {f"EMU_STRATEGY_{k.upper()}": v for k, v in emu.STRATEGIES.items()} == strategies
     st = _declared_enum("EMU_STATUS_")
     assert {v: k for k, v in st.items()} == emu.STATUS_NAMES
 
@@ -96,3 +101,33 @@ def test_no_gpu_means_error_not_fallback(lib):
     aligned = ctypes.c_void_p((ctypes.cast(buf, ctypes.c_void_p).value + 15) & ~15)
     st = f(0, 0, 0, 4, 4, 4, 1.0, aligned, 4, aligned, 4, 0.0, aligned, 4, ctypes.c_void_p(0))
     assert st in (3, 5)
+
+
+def test_strategy_and_dispatch_are_host_decisions(lib):
+    """The strategy switch and the dispatch decision need no GPU.  Eager runs
+    every product in the requested mode; performant sends small products to
+    native FP32 and keeps large ones emulated; FP32 requested stays FP32;
+    packing has no FP32 form."""
+    assert emu.emu_get_strategy() == "eager"
+    assert emu.load().emu_set_strategy(7) == 1
+    for mode in ("bf16x9", "tf32x3", "tf32x1", "bf16x6", "fp32"):
+        assert emu.emu_dispatch_query(mode, 64, 64, 64) == mode
+        assert emu.emu_dispatch_query(mode, 16384, 16384, 16384) == mode
+    with emu.strategy("performant"):
+        assert emu.emu_get_strategy() == "performant"
+        for mode in ("bf16x9", "tf32x3"):
+            assert emu.emu_dispatch_query(mode, 64, 64, 64) == "fp32"
+            assert emu.emu_dispatch_query(mode, 192, 256, 256) == "fp32"
+            assert emu.emu_dispatch_query(mode, 16384, 16384, 16384) == mode
+            assert emu.emu_dispatch_query(mode, 17280, 512, 512) == mode
+        assert emu.emu_dispatch_query("fp32", 16384, 16384, 16384) == "fp32"
+        # a larger product is never sent to native FP32 when a smaller one of
+        # the same shape family stays emulated
+        sizes = [64 * 2 ** i for i in range(9)]
+        picks = [emu.emu_dispatch_query("bf16x9", s, s, s) for s in sizes]
+        first_emulated = picks.index("bf16x9")
+        assert all(p == "bf16x9" for p in picks[first_emulated:])
+    assert emu.emu_get_strategy() == "eager"
+    with pytest.raises(emu.EmuError):
+        emu.emu_dispatch_query("bf16x9", 0, 4, 4)
+    assert emu.emu_pack_bytes("fp32", 64, 64) == -1

@@ -1,0 +1,97 @@
+"""Native FP32 (EMU_MODE_FP32) and the performant strategy on the GPU.
+
+The native path computes each output as one chain of fmaf over k in
+ascending order, then the epilogue, which is the oracle's plain FP32 SGEMM
+by definition, so every element must carry the same bits.  Under the
+performant strategy a small product requested in an emulated mode must give
+the native bits, and a large one the emulated bits of the eager strategy.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from tests import _gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _same_bits(got, want):
+    got, want = np.asarray(got, np.float32), np.asarray(want, np.float32)
+    diff = got.view(np.uint32) != want.view(np.uint32)
+    assert not diff.any(), f"{int(diff.sum())} of {diff.size} elements differ, e.g. {got[diff][:3]} vs {want[diff][:3]}"
+
+
+@pytest.mark.parametrize("tA,tB", [(False, False), (True, False), (False, True), (True, True)])
+# micro-tiles: 1 x 1 per thread for the small outputs, 2 x 2 for (1030, 645),
+# 4 x 4 for (2050, 1283) (the library picks the largest that fills the SMs)
+@pytest.mark.parametrize("M,N,K", [(300, 260, 200), (64, 1000, 37), (130, 70, 1), (65, 64, 16), (1, 5, 1000),
+                                   (1030, 645, 45), (2050, 1283, 40)])
+def test_native_fp32_matches_oracle_bitwise(tA, tB, M, N, K):
+    rng = np.random.default_rng(41)
+    A = rng.standard_normal((K, M) if tA else (M, K)).astype(np.float32)
+    B = rng.standard_normal((N, K) if tB else (K, N)).astype(np.float32)
+    Cold = rng.standard_normal((M, N)).astype(np.float32)
+    C = _gpu.gpu_sgemm("fp32", A, B, transA=tA, transB=tB, alpha=0.75, beta=-0.5, C_old=Cold)
+    p = oracle.Problem(A, B, transA=tA, transB=tB, alpha=0.75, beta=-0.5, C_old=Cold)
+    _same_bits(C, oracle.sgemm_f32(p))
+    # beta == 0 never reads C (the helper fills it with NaN)
+    _same_bits(_gpu.gpu_sgemm("fp32", A, B, transA=tA, transB=tB),
+               oracle.sgemm_f32(oracle.Problem(A, B, transA=tA, transB=tB)))
+
+
+def test_native_fp32_order_and_fusion():
+    """Cases whose bits depend on the order of the k-chain and on fusing the
+    multiply into the add (k ascending, one rounding per step)."""
+    A = np.array([[2.0 ** 24, 1.0, -2.0 ** 24], [-(1 + 2.0 ** -11), 1 + 2.0 ** -12, 0.0]], np.float32)
+    B = np.array([[1.0, 1.0], [1.0, 1 + 2.0 ** -12], [1.0, 0.0]], np.float32)
+    C = _gpu.gpu_sgemm("fp32", A, B)
+    assert C[0, 0] == 0.0 and C[1, 1] == 2.0 ** -24
+    _same_bits(C, oracle.sgemm_f32(oracle.Problem(A, B)))
+
+
+def test_native_linear_layer_matches_oracle_bitwise():
+    import fp32_emulated_gemm_gb300 as emu
+    rng = np.random.default_rng(42)
+    M, N, K = 333, 100, 72
+    X = rng.standard_normal((M, K)).astype(np.float32)
+    Wt = rng.standard_normal((N, K)).astype(np.float32)
+    b = rng.standard_normal(N).astype(np.float32)
+    dY = rng.standard_normal((M, N)).astype(np.float32)
+    dW0 = rng.standard_normal((N, K)).astype(np.float32)
+    Y = emu.linear_fwd(_gpu.to_dev(X), _gpu.to_dev(Wt), _gpu.to_dev(b), mode="fp32")
+    dX = emu.linear_bwd_input(_gpu.to_dev(dY), _gpu.to_dev(Wt), mode="fp32")
+    dW = emu.linear_bwd_weight(_gpu.to_dev(dY), _gpu.to_dev(X), mode="fp32", out=_gpu.to_dev(dW0), beta=1.0)
+    assert emu.emu_stream_check() == 0
+    _same_bits(Y.cpu().numpy(), oracle.sgemm_f32(oracle.Problem(X, Wt, transB=True, bias=b)))
+    _same_bits(dX.cpu().numpy(), oracle.sgemm_f32(oracle.Problem(dY, Wt)))
+    _same_bits(dW.cpu().numpy(), oracle.sgemm_f32(oracle.Problem(dY, X, transA=True, beta=1.0, C_old=dW0)))
+
+
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
+def test_performant_strategy_small_native_large_emulated(mode):
+    import fp32_emulated_gemm_gb300 as emu
+    rng = np.random.default_rng(43)
+    small, large = (192, 256, 256), (2048, 1536, 512)
+    out = {}
+    for name, (M, N, K) in (("small", small), ("large", large)):
+        A = rng.standard_normal((M, K)).astype(np.float32)
+        B = rng.standard_normal((K, N)).astype(np.float32)
+        eager = _gpu.gpu_sgemm(mode, A, B)
+        with emu.strategy("performant"):
+            chosen = emu.emu_dispatch_query(mode, M, N, K)
+            perf = _gpu.gpu_sgemm(mode, A, B)
+        out[name] = chosen
+        if chosen == "fp32":
+            _same_bits(perf, oracle.sgemm_f32(oracle.Problem(A, B)))
+        else:
+            _same_bits(perf, eager)
+    assert out == {"small": "fp32", "large": mode}
+    assert emu.emu_get_strategy() == "eager"
+
+
+def test_packed_calls_reject_native_mode():
+    import torch
+    import fp32_emulated_gemm_gb300 as emu
+    B = torch.zeros((64, 64), device="cuda")
+    with pytest.raises((emu.EmuError, KeyError, ValueError)):
+        emu.pack_b(B, mode="fp32")

@@ -86,6 +86,25 @@ def test_sgemm_f32_within_summation_bound():
             assert np.array_equal(C, (A.astype(np.float64) @ B.astype(np.float64)).astype(np.float32))
 
 
+def test_sgemm_f32_is_one_fused_chain_in_k_order():
+    """Native FP32 is defined as acc = fmaf(a_k, b_k, acc) for k = 0, 1, ...
+    from +0.  Row 0: 2^24 + 1 rounds back to 2^24 (tie to even) before
+    -2^24 arrives, so the ascending chain gives 0 (descending would give 1).
+    Row 1: (1 + 2^-12)^2 - (1 + 2^-11) = 2^-24 survives only when the
+    multiply is fused into the add."""
+    A = np.array([[2.0 ** 24, 1.0, -2.0 ** 24], [-(1 + 2.0 ** -11), 1 + 2.0 ** -12, 0.0]], np.float32)
+    B = np.array([[1.0, 1.0], [1.0, 1 + 2.0 ** -12], [1.0, 0.0]], np.float32)
+    C = oracle.sgemm_f32(oracle.Problem(A, B))
+    assert C[0, 0] == 0.0
+    assert C[1, 1] == 2.0 ** -24
+    # epilogue: fmaf(alpha, acc, beta * C_old) + bias, one rounding for alpha acc + beta C_old
+    acc = np.float32(1 + 2.0 ** -12)
+    Cold = np.array([[-(1 + 2.0 ** -11)]], np.float32)
+    p = oracle.Problem(np.array([[acc]], np.float32), np.array([[1.0]], np.float32), alpha=float(acc), beta=1.0,
+                       C_old=Cold, bias=np.array([0.5], np.float32))
+    assert oracle.sgemm_f32(p)[0, 0] == np.float32(2.0 ** -24 + 0.5)
+
+
 # -------------------------------------------------------------- BF16x9 ------
 def _band_exact(a, b):
     """Exact band sums from the (separately pinned) split: T_b = sum over

@@ -90,3 +90,27 @@ def test_plan_query_rejects_bad_arguments():
         with pytest.raises(emu.EmuError) as e:
             emu.emu_plan_query(*args)
         assert e.value.status == 1
+
+
+def _cost(plan, pairs):
+    """Predicted time in pipeline stages, from the plan's own fields: waves
+    of units, each its k-stages plus 3 stages of output stores, plus 1.5
+    stages of reduction when a tile is split."""
+    T, KS = plan["tiles_m"] * plan["tiles_n"], plan["k_stages"]
+    Sa, Sb = plan["split_a"], plan["split_b"]
+    if Sb == 1 and plan["tiles_a"] == T:
+        units = T * Sa
+        used = pairs if (units <= pairs or Sa == 1) else pairs // Sa * Sa
+        return -(-units // used) * (-(-KS // Sa) + 3) + (1.5 if Sa > 1 else 0.0)
+    W = plan["tiles_a"] // pairs
+    return W * (KS + 3) + (-(-KS // Sb) + 3) + 1.5
+
+
+@pytest.mark.parametrize("M,N,K", [(6144, 1024, 256), (6144, 256, 1024), (552960, 1024, 256), (64, 64, 64),
+                                   (1536, 256, 1024), (2048, 2048, 2048), (19 * 256, 4 * 256, 4096)])
+def test_plan_cost_is_reported_and_no_worse_than_unsplit(M, N, K):
+    plan = emu.emu_plan_query(M, N, K, GB300_PAIRS)
+    c = _cost(plan, GB300_PAIRS)
+    assert abs(plan["cost_x100"] / 100.0 - c) <= 0.006
+    T, KS = plan["tiles_m"] * plan["tiles_n"], plan["k_stages"]
+    assert c <= -(-T // GB300_PAIRS) * (KS + 3) + 1e-9
