@@ -544,8 +544,9 @@ int env_int(const char* name, int dflt) {
 //     use are a multiple of S, so that waves hold whole tiles;
 //   hybrid: W full waves of whole tiles on all pairs, then the remaining
 //     tiles (fewer than the pairs) in S pieces, one more wave at most.
-// EMU_SPLIT_K (uniform S) and EMU_PIPE (0 short-k, 1 long-k) override the
-// choice, for diagnostics and tuning.
+// EMU_SPLIT_K (uniform S), EMU_SPLIT_TAIL (hybrid with that S for the
+// remaining tiles, where a hybrid plan exists) and EMU_PIPE (0 short-k,
+// 1 long-k) override the choice, for diagnostics and tuning.
 Plan make_plan(int64_t M, int64_t N, int64_t K, int pairs) {
     Plan plan{};
     plan.tn = 256;
@@ -568,8 +569,16 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int pairs) {
         return (double)waves * ((KS + S - 1) / S + kStoreStages) + (S > 1 ? kReduceStages : 0.0);
     };
     const int force_split = env_int("EMU_SPLIT_K", 0);
+    const int force_tail = env_int("EMU_SPLIT_TAIL", 0);
     const int s_max = KS < 32 ? KS : 32;
-    if (force_split >= 1) {
+    const long long W0 = T / pairs, tail0 = T - W0 * pairs;
+    if (force_split < 1 && force_tail >= 2 && W0 >= 1 && tail0 >= 1 && force_tail <= s_max &&
+        tail0 * force_tail <= pairs) {
+        const int S = force_tail;
+        plan.tiles_a = (int)(W0 * pairs); plan.split_a = 1; plan.split_b = S;
+        plan.clusters = pairs;
+        plan.cost = (double)W0 * (KS + kStoreStages) + ((KS + S - 1) / S + kStoreStages) + kReduceStages;
+    } else if (force_split >= 1) {
         int S = force_split < s_max ? force_split : s_max;
         S = S < pairs ? S : pairs;
         set_uniform(S);

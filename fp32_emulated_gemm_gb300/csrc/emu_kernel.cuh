@@ -430,9 +430,8 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
     // allocates TMEM (the load latency overlaps the set-up).  Like every
     // global access of this kernel they wait for the grids this launch
     // depends on.
-    auto issue_load = [&](int s, int tile, int ks) {
-        const int m0 = (tile / p.tiles_n) * TILE_M + HALF * rank;
-        const int n0 = (tile % p.tiles_n) * TN + BH * rank;
+    // (m0, n0): this CTA's first row of op(A) and of op(B)^T in the tile
+    auto issue_load_at = [&](int s, int m0, int n0, int ks) {
         uint64_t* full = &fp32_full[s];
         mbar_arrive_expect_tx(full, KC::FP32_STAGE);
         uint8_t* dA = fp32_ring + s * KC::FP32_STAGE;
@@ -445,14 +444,19 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
             else for (int j = 0; j < BH / 32; ++j) tma_load_2d(dB + j * 4096, &p.tmB, full, n0 + 32 * j, k0);
         }
     };
+    auto issue_load = [&](int s, int tile, int ks) {
+        issue_load_at(s, (tile / p.tiles_n) * TILE_M + HALF * rank, (tile % p.tiles_n) * TN + BH * rank, ks);
+    };
     // packed shapes: op(B)'s component tiles of a stage, straight into the
     // component ring (box {32 k, BH rows, 1 component} per component)
-    auto issue_bload = [&](int bslot, int tile, int ks) {
-        const int n0 = (tile % p.tiles_n) * TN + BH * rank;
+    auto issue_bload_at = [&](int bslot, int n0, int ks) {
         uint64_t* full = &bcomp_full[bslot];
         mbar_arrive_expect_tx(full, KC::BCOMP_BYTES);
         uint8_t* dst = bcomp_ring + bslot * KC::BCOMP_BYTES;
         for (int c = 0; c < C::NCOMP; ++c) tma_load_3d(dst + c * KC::COMP_B, &p.tmB, full, ks * BK, n0, c);
+    };
+    auto issue_bload = [&](int bslot, int tile, int ks) {
+        issue_bload_at(bslot, (tile % p.tiles_n) * TN + BH * rank, ks);
     };
     int early = 0, early_b = 0;  // stages already issued by thread 0 (warp 0 lane 0, the producer)
     if (threadIdx.x == 0) {
@@ -465,15 +469,59 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         for (int s = 0; s < NB; ++s) { mbar_init(&bcomp_full[s], 1); mbar_init(&bcomp_empty[s], 1); }
         *abort_flag = 0;
         fence_mbar_init();
-        griddep_wait();
-        const int early_bmax = PACKED ? NB : 0;
-        for (int u = cid; (early < NF || early_b < early_bmax) && u < p.num_units; u += ncl) {
-            const Unit w = unit_of(p, u);
-            for (int ks = w.kb; (early < NF || early_b < early_bmax) && ks < w.ke; ++ks) {
-                if (early < NF) issue_load(early++, w.tile, ks);
-                if (early_b < early_bmax) issue_bload(early_b++, w.tile, ks);
+        // Where the first stages come from depends on the parameters alone:
+        // it is worked out before waiting for the previous grid, so that the
+        // unit arithmetic and the parameter reads (about a microsecond) do
+        // not delay the first loads.
+        constexpr int NE = PACKED && NB > NF ? NB : NF;
+        int e_m0[NE], e_n0[NE], e_ks[NE], ne = 0;
+        {
+            int u = cid, ks = 0, ke = 0, tile = 0;
+#pragma unroll
+            for (int i = 0; i < NE; ++i) {
+                while (ks >= ke && u < p.num_units) {
+                    const Unit w = unit_of(p, u);
+                    tile = w.tile; ks = w.kb; ke = w.ke;
+                    u += ncl;
+                }
+                if (ks < ke) {
+                    e_m0[i] = (tile / p.tiles_n) * TILE_M + HALF * rank;
+                    e_n0[i] = (tile % p.tiles_n) * TN + BH * rank;
+                    e_ks[i] = ks++;
+                    ne = i + 1;
+                }
             }
         }
+        // the first stages' operands are prefetched into L2 while the
+        // previous grid finishes (L2 is coherent, so nothing stale is read)
+#pragma unroll
+        for (int i = 0; i < NE; ++i) {
+            if (i < ne) {
+                const int k0 = e_ks[i] * BK;
+                if (i < NF) {
+                    if (!p.a_mn_major) tma_prefetch_l2_2d(&p.tmA, k0, e_m0[i]);
+                    else for (int j = 0; j < HALF / 32; ++j) tma_prefetch_l2_2d(&p.tmA, e_m0[i] + 32 * j, k0);
+                    if constexpr (!PACKED) {
+                        if (!p.b_mn_major) tma_prefetch_l2_2d(&p.tmB, k0, e_n0[i]);
+                        else for (int j = 0; j < BH / 32; ++j) tma_prefetch_l2_2d(&p.tmB, e_n0[i] + 32 * j, k0);
+                    }
+                }
+                if constexpr (PACKED) {
+                    if (i < NB)
+                        for (int c = 0; c < C::NCOMP; ++c) tma_prefetch_l2_3d(&p.tmB, k0, e_n0[i], c);
+                }
+            }
+        }
+        griddep_wait();
+#pragma unroll
+        for (int i = 0; i < NE; ++i) {
+            if (i < ne) {
+                if (i < NF) issue_load_at(i, e_m0[i], e_n0[i], e_ks[i]);
+                if (PACKED && i < NB) issue_bload_at(i, e_n0[i], e_ks[i]);
+            }
+        }
+        early = ne < NF ? ne : NF;
+        early_b = PACKED ? (ne < NB ? ne : NB) : 0;
     }
     if (warp == WARP_MMA) {
         tmem_alloc_pair(tmem_slot, TMEM_COLS);

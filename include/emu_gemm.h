@@ -263,8 +263,8 @@ emu_status_t emu_selftest_wait_timeout(uint64_t budget_ns, emu_stream_t stream);
 /*
  * emu_plan_query -- diagnostic, host only (no GPU, no CUDA call): the launch
  * plan emu_sgemm would use for an M x N x K product on a device with `pairs`
- * co-resident CTA pairs (76 on a GB300), honouring the EMU_SPLIT_K and
- * EMU_PIPE overrides.  Writes EMU_PLAN_FIELDS values to out[0..]:
+ * co-resident CTA pairs (76 on a GB300), honouring the EMU_SPLIT_K,
+ * EMU_SPLIT_TAIL and EMU_PIPE overrides.  Writes EMU_PLAN_FIELDS values to out[0..]:
  *   0 pipeline shape (0 short-k, 1 long-k)   1 tile width (256)
  *   2 tiles along M (256 rows each)          3 tiles along N
  *   4 k-stages (32 each)                     5 tiles processed first (tiles_a)

@@ -66,3 +66,43 @@ def test_pet_small_layer_matches_tensor_core_model(mode, monkeypatch):
     assert emu.emu_stream_check() == 0
     _same_bits(Y.cpu().numpy()[rows], oracle.gemm_tc(oracle.Problem(X, Wt, transB=True, bias=b), mode=mode, rows=rows))
     _same_bits(dX.cpu().numpy()[rows], oracle.gemm_tc(oracle.Problem(dY, Wt), mode=mode, rows=rows))
+
+
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
+def test_multiwave_split_plan_matches_tensor_core_model(mode, monkeypatch):
+    """96 units of a forced 4-way split on 76 pairs: two waves of split
+    tiles, so some pairs reduce a split tile and then go on to another unit.
+    Rows sampled from every tile row."""
+    import fp32_emulated_gemm_gb300 as emu
+    monkeypatch.setenv("EMU_SPLIT_K", "4")
+    M, N, K = 1536, 1024, 512
+    plan = emu.emu_plan_query(M, N, K, 76)
+    assert plan["split_a"] == 4 and plan["units"] > plan["pairs"]
+    rng = np.random.default_rng(24)
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    B = rng.standard_normal((K, N)).astype(np.float32)
+    rows = W.sample_rows(M, every=61, edge=2)
+    C = _gpu.gpu_sgemm(mode, A, B)
+    _same_bits(C[rows], oracle.gemm_tc(oracle.Problem(A, B), mode=mode, rows=rows, pieces=4))
+
+
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
+def test_hybrid_plan_matches_tensor_core_model(mode):
+    """The library's own plan for the PET-small forward pass: whole tiles in
+    the first wave, the tail tiles split.  Rows of whole tiles follow the
+    unsplit model, rows of tail tiles the split one."""
+    import fp32_emulated_gemm_gb300 as emu
+    s = W.PET_SMALL
+    plan = emu.emu_plan_query(s.M, s.N, s.K, 76)
+    assert plan["split_a"] == 1 and plan["split_b"] > 1 and plan["tiles_a"] % plan["tiles_n"] == 0
+    first_split_row = plan["tiles_a"] // plan["tiles_n"] * 256
+    X, Wt, b, _ = W.linear_inputs(s, W.CONFIG_ID["pet_small"])
+    Y = emu.linear_fwd(_gpu.to_dev(X), _gpu.to_dev(Wt), _gpu.to_dev(b), mode=mode)
+    assert emu.emu_stream_check() == 0
+    Y = Y.cpu().numpy()
+    rows = W.sample_rows(s.M, every=89, edge=3)
+    p = oracle.Problem(X, Wt, transB=True, bias=b)
+    whole, tail = rows[rows < first_split_row], rows[rows >= first_split_row]
+    assert len(whole) and len(tail)
+    _same_bits(Y[whole], oracle.gemm_tc(p, mode=mode, rows=whole, pieces=1))
+    _same_bits(Y[tail], oracle.gemm_tc(p, mode=mode, rows=tail, pieces=plan["split_b"]))
