@@ -43,12 +43,17 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-comparators", action="store_true")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="replace the workload's M (token rows) by this many, for profiler captures of a "
+                         "smaller case of the same kernel; the JSON line names the changed workload")
     return ap.parse_args()
 
 
-def shape_of(name):
+def shape_of(name, rows=0):
+    import dataclasses
     from fp32_emulated_gemm_gb300 import workloads as W
-    return {"pet_small": W.PET_SMALL, "pet_large": W.PET_LARGE, "wide_l1": W.WIDE_L1, "wide_l2": W.WIDE_L2}[name]
+    s = {"pet_small": W.PET_SMALL, "pet_large": W.PET_LARGE, "wide_l1": W.WIDE_L1, "wide_l2": W.WIDE_L2}[name]
+    return dataclasses.replace(s, M=rows) if rows > 0 else s
 
 
 def config_id(name):
@@ -169,7 +174,7 @@ def run_reference(args, world, rank):
     import oracle
     from fp32_emulated_gemm_gb300 import workloads as W
     oracle.build()
-    s = shape_of(args.workload)
+    s = shape_of(args.workload, args.rows)
     X, Wt, b, dY = W.linear_inputs(s, config_id(args.workload), rows=64)
     r = 8  # rows per step: keeps --steps K runs within minutes
 
@@ -219,7 +224,7 @@ def main():
     emu_build.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    s = shape_of(args.workload)
+    s = shape_of(args.workload, args.rows)
     mode = emu.MODES[args.mode]
     X, Wt, b, dY = W.linear_inputs(s, config_id(args.workload))
     Xd, Wd, bd, dYd = (torch.from_numpy(a).to(dev) for a in (X, Wt, b, dY))
@@ -393,6 +398,8 @@ def load_traffic(args):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary for this workload, or None when no capture exists or the kernel
     sources changed since the counters were taken."""
+    if args.rows:
+        return None  # the committed counters are for the full workload
     path = os.path.join(ROOT, "profiles", f"traffic_{args.workload}_{args.mode}.json")
     try:
         with open(path) as f:
