@@ -325,7 +325,53 @@ def main():
         line["cpu_baseline"] = cpu_baseline(s, args.mode)
     if not args.no_comparators:
         line["comparators"] = cublas_comparators(s)
+        line["extras"] = extra_passes(emu, mode, s, Xd, dYd, flush, stream, fwd, bwd, peak)
     print(json.dumps(line), flush=True)
+
+
+def extra_passes(emu, mode, s, Xd, dYd, flush, stream, fwd, bwd, peak, n=100):
+    """Context beside the headline, after the timed region: the emulated
+    weight gradient dW = dY^T X of the same layer (one launch, L2 flushed
+    before it), and the step with L2 warm (50 steps back to back between one
+    event pair: inputs and outputs stay in L2, as in steady-state inference)."""
+    import torch
+    sp = stream.cuda_stream
+    dW = torch.empty((s.N, s.K), device=Xd.device)
+
+    def wgrad():
+        emu.emu_linear_bwd_weight(mode, s.M, s.N, s.K, dYd, Xd, 0.0, dW, sp)
+
+    for _ in range(3):
+        wgrad()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for i in range(n):
+        flush.fill_(1.0)
+        ev[i][0].record(stream)
+        wgrad()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    wg_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / n
+    wg_tf = 2.0 * s.M * s.N * s.K / (wg_ms * 1e-3) / 1e12
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(5):
+        fwd()
+        bwd()
+    e0.record(stream)
+    warm = 50
+    for _ in range(warm):
+        fwd()
+        bwd()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    st = emu.emu_stream_check(sp)
+    if st != 0:
+        raise RuntimeError(emu.emu_status_string(st))
+    warm_ms = e0.elapsed_time(e1) / warm
+    warm_tf = step_flops(s) / (warm_ms * 1e-3) / 1e12
+    return {"weight_grad": {"value": wg_tf, "unit": "TFLOPS", "ms": wg_ms, "frac": wg_tf / peak,
+                            "pass": f"dW[{s.N},{s.K}] = dY^T X, contraction over M={s.M}, L2 flushed"},
+            "warm_step": {"value": warm_tf, "unit": "TFLOPS", "ms_per_step": warm_ms, "frac": warm_tf / peak,
+                          "l2": "warm (50 steps back to back)"}}
 
 
 def isolated_launch_ms(stream, flush, fwd, bwd, n):
