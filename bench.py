@@ -314,7 +314,7 @@ def main():
                      "kernel": f"emu_gemm_kernel<{args.mode}>",
                      "launch_ms": step_ms / 2,
                      "isolated_fwd_ms": fwd_ms, "isolated_bwd_ms": bwd_ms},
-        "gpu_launches": 2 * K,
+        "gpu_launches": launches_per_step(emu, args.mode, s) * K,
         "wall_s_timed_region": wall,
     }
     if clocks:
@@ -327,6 +327,19 @@ def main():
         line["comparators"] = cublas_comparators(s)
         line["extras"] = extra_passes(emu, mode, s, Xd, dYd, flush, stream, fwd, bwd, peak)
     print(json.dumps(line), flush=True)
+
+
+def launches_per_step(emu, mode, s):
+    """Kernels one step launches: one per GEMM, plus, in the TF32 modes, the
+    library's split of op(B) ahead of a product whose op(A) spans four or
+    more 256-row tiles (unless EMU_AUTOPACK=0)."""
+    n = 0
+    for (m, n_out, k) in ((s.M, s.N, s.K), (s.M, s.K, s.N)):   # forward, input gradient
+        n += 1
+        if (mode in ("tf32x3", "tf32x1") and os.environ.get("EMU_AUTOPACK", "1") != "0"
+                and -(-m // 256) >= 4 and emu.emu_pack_bytes(mode, n_out, k) <= (1 << 30)):
+            n += 1
+    return n
 
 
 def extra_passes(emu, mode, s, Xd, dYd, flush, stream, fwd, bwd, peak, n=100):
