@@ -31,6 +31,7 @@ def run_pins():
             g.test_bf16x9_gemm_against_exact_rationals(v, tA, tB)
     g.test_f64_gemm_small_integers_exact_golden()
     g.test_sgemm_f32_within_summation_bound()
+    g.test_sgemm_f32_is_one_fused_chain_in_k_order()
     g.test_bf16x9_bands_hold_the_nine_products()
     g.test_tf32x3_terms_are_the_three_products()
     g.test_tf32x3_drops_lo_times_lo_closed_form()

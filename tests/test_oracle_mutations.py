@@ -38,6 +38,10 @@ MUTANTS = {
                              "s += (double)(float)((double)ar[k] * (double)br[k]);"),
     "sgemm_first_term_dropped": ("acc = fmaf(ar[k], br[k], acc);",
                                  "acc = (k == 0) ? 0.0f : fmaf(ar[k], br[k], acc);"),
+    "sgemm_unfused": ("acc = fmaf(ar[k], br[k], acc);",
+                      "acc = acc + (float)((double)ar[k] * (double)br[k]);"),
+    "sgemm_descending_k": ("for (int64_t k = 0; k < K; ++k) acc = fmaf(ar[k], br[k], acc);",
+                           "for (int64_t k = K - 1; k >= 0; --k) acc = fmaf(ar[k], br[k], acc);"),
     "bias_dropped": ("if (bias_elem) c = c + *bias_elem;", ";"),
     "bf16x6_band1_scale": ("            acc = acc + S[1] * 0x1p-8f;\n            acc = acc + S[0];",
                            "            acc = acc + S[1] * 0x1p-7f;\n            acc = acc + S[0];"),
