@@ -83,6 +83,18 @@ def test_overrides(monkeypatch):
     monkeypatch.delenv("EMU_SPLIT_K")
     monkeypatch.setenv("EMU_PIPE", "1")
     assert emu.emu_plan_query(6144, 1024, 256, GB300_PAIRS)["pipe"] == 1
+    monkeypatch.delenv("EMU_PIPE")
+    auto = emu.emu_plan_query(6144, 1024, 256, GB300_PAIRS)
+    monkeypatch.setenv("EMU_SPLIT_TAIL", "2")       # hybrid tail in 2 pieces
+    p = emu.emu_plan_query(6144, 1024, 256, GB300_PAIRS)
+    assert (p["tiles_a"], p["split_a"], p["split_b"], p["units"]) == (76, 1, 2, 116)
+    _check_invariants(6144, 1024, 256, GB300_PAIRS, p)
+    monkeypatch.setenv("EMU_SPLIT_TAIL", "4")       # 20 tail tiles x 4 > 76 pairs: not a valid wave, ignored
+    assert emu.emu_plan_query(6144, 1024, 256, GB300_PAIRS) == auto
+    monkeypatch.delenv("EMU_SPLIT_TAIL")
+    dx = emu.emu_plan_query(6144, 256, 1024, GB300_PAIRS)
+    monkeypatch.setenv("EMU_SPLIT_TAIL", "2")       # 24 tiles < 76 pairs: no hybrid plan exists, ignored
+    assert emu.emu_plan_query(6144, 256, 1024, GB300_PAIRS) == dx
 
 
 def test_plan_query_rejects_bad_arguments():
