@@ -273,17 +273,20 @@ __global__ void pack_kernel(int64_t rows, int64_t K, const float* B, int64_t ldb
 // then C = fmaf(alpha, acc, beta * C_old) (beta == 0: C_old not read), plus
 // the bias when there is one.  A block of 16 x 16 threads computes a 16R x 16R
 // tile of C, R x R outputs per thread (rows R ty + i, columns R tx + j), from
-// 16-deep k-slices of op(A) and op(B) staged in shared memory.  The chains
+// k-slices of depth KT = 64 / R staged in shared memory (the smaller the
+// tile, the longer the slice: fewer load round trips per chain).  The chains
 // cannot be split along k, so small outputs take a smaller R to occupy the SMs.
-constexpr int NAT_KT = 16, NAT_MAX_GRID_Y = 65535;
+constexpr int NAT_MAX_GRID_Y = 65535;
 template <int R>
 __global__ void __launch_bounds__(256) native_sgemm_kernel(int M, int N, int K, float alpha, const float* A,
                                                            long long lda, int a_mn, const float* B, long long ldb,
                                                            int b_mn, float beta, float* C, long long ldc,
                                                            const float* bias) {
     constexpr int T = 16 * R, LD = T + 4;  // +4: fewer bank conflicts, rows stay 16-byte aligned
-    __shared__ __align__(16) float As[NAT_KT][LD];
-    __shared__ __align__(16) float Bs[NAT_KT][LD];
+    constexpr int KT = 64 / R;             // slice depth
+    constexpr int NQ = KT * T / 256;       // elements of each operand's slice per thread (4)
+    __shared__ __align__(16) float As[KT][LD];
+    __shared__ __align__(16) float Bs[KT][LD];
     const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
     const int m0 = blockIdx.x * T, n0 = blockIdx.y * T;
     float acc[R][R];
@@ -291,20 +294,20 @@ __global__ void __launch_bounds__(256) native_sgemm_kernel(int M, int N, int K, 
     for (int i = 0; i < R; ++i)
 #pragma unroll
         for (int j = 0; j < R; ++j) acc[i][j] = 0.0f;
-    // each slice is 16 x T elements, R per thread: element e = threadIdx.x + 256 q
-    // is (k, r) = (e / T, e % T) for an MN-major source and (e % 16, e / 16)
+    // each slice is KT x T elements, NQ per thread: element e = threadIdx.x + 256 q
+    // is (k, r) = (e / T, e % T) for an MN-major source and (e % KT, e / KT)
     // for a K-major one, so that neighbouring threads read neighbouring
     // addresses.  The next slice is fetched into registers while the current
     // one is used.
-    float ra_[R], rb_[R];
+    float ra_[NQ], rb_[NQ];
     auto fetch = [&](int k0) {
 #pragma unroll
-        for (int q = 0; q < R; ++q) {
+        for (int q = 0; q < NQ; ++q) {
             const int e = threadIdx.x + 256 * q;
-            const int ka = a_mn ? e / T : e % 16, ra = a_mn ? e % T : e / 16;
+            const int ka = a_mn ? e / T : e % KT, ra = a_mn ? e % T : e / KT;
             const int gm = m0 + ra, gka = k0 + ka;
             ra_[q] = (gm < M && gka < K) ? A[a_mn ? (long long)gka * lda + gm : (long long)gm * lda + gka] : 0.0f;
-            const int kb = b_mn ? e / T : e % 16, cb = b_mn ? e % T : e / 16;
+            const int kb = b_mn ? e / T : e % KT, cb = b_mn ? e % T : e / KT;
             const int gn = n0 + cb, gkb = k0 + kb;
             rb_[q] = (gn < N && gkb < K) ? B[b_mn ? (long long)gkb * ldb + gn : (long long)gn * ldb + gkb] : 0.0f;
         }
@@ -331,18 +334,18 @@ __global__ void __launch_bounds__(256) native_sgemm_kernel(int M, int N, int K, 
             for (int j = 0; j < R; ++j) acc[i][j] = __fmaf_rn(av[i], bv[j], acc[i][j]);
     };
     if (K > 0) fetch(0);
-    for (int k0 = 0; k0 < K; k0 += NAT_KT) {
+    for (int k0 = 0; k0 < K; k0 += KT) {
 #pragma unroll
-        for (int q = 0; q < R; ++q) {
+        for (int q = 0; q < NQ; ++q) {
             const int e = threadIdx.x + 256 * q;
-            As[a_mn ? e / T : e % 16][a_mn ? e % T : e / 16] = ra_[q];
-            Bs[b_mn ? e / T : e % 16][b_mn ? e % T : e / 16] = rb_[q];
+            As[a_mn ? e / T : e % KT][a_mn ? e % T : e / KT] = ra_[q];
+            Bs[b_mn ? e / T : e % KT][b_mn ? e % T : e / KT] = rb_[q];
         }
         __syncthreads();
-        if (k0 + NAT_KT < K) fetch(k0 + NAT_KT);
-        if (K - k0 >= NAT_KT) {
+        if (k0 + KT < K) fetch(k0 + KT);
+        if (K - k0 >= KT) {
 #pragma unroll
-            for (int k = 0; k < NAT_KT; ++k) step(k);
+            for (int k = 0; k < KT; ++k) step(k);
         } else {
             for (int k = 0; k < K - k0; ++k) step(k);  // only k < K enters the chains
         }
@@ -398,11 +401,12 @@ std::atomic<int> g_strategy{EMU_STRATEGY_EAGER};
 
 // Predicted GPU times in microseconds on GB300, fitted to measured kernel
 // times (CUDA graphs of back-to-back calls, 66 shapes from 64^3 to 2048^3,
-// rms error about 6% emulated and 12% native).  Emulated: a fixed start-up,
+// rms error about 6% emulated and 14% native).  Emulated: a fixed start-up,
 // the plan's pipeline stages (waves x (k-stages + stores)) at the mode's
 // stage time, and for split tiles a reduction that grows with the pieces per
-// tile.  Native: a fixed cost plus one step per 16-deep k-slice, whose time
-// grows with the FMAs each SM carries per slice.
+// tile.  Native: a fixed cost plus, per k of the chains, a latency term that
+// depends on the micro-tile and a throughput term that grows with the FMAs
+// each SM carries.
 struct EmuTimeModel { double fixed, stage, split_fixed, split_per_piece; };
 EmuTimeModel emu_time_model(emu_mode_t mode) {
     switch (mode) {
@@ -414,7 +418,9 @@ EmuTimeModel emu_time_model(emu_mode_t mode) {
         default: return {3.8, 0.8, 2.64, 0.51};  // TF32x1
     }
 }
-constexpr double kNatFixedUs = 1.6, kNatSliceUs = 0.342, kNatSlicePerSmFmaUs = 0.0479 / (256.0 * 16.0);
+constexpr double kNatFixedUs = 1.46, kNatPerFmaPerSmUs = 1.105e-5;
+// per k of the chain, by micro-tile size R = 1, 2, 4
+double nat_per_k_us(int R) { return R == 1 ? 0.0172 : R == 2 ? 0.0254 : 0.0292; }
 
 __global__ void scale_kernel(int64_t M, int64_t N, float beta, float* C, int64_t ldc, const float* bias) {
     const int64_t total = M * N;
@@ -626,8 +632,8 @@ emu_mode_t dispatch_mode(emu_mode_t mode, int64_t M, int64_t N, int64_t K, int p
                           (S > 1 ? em.split_fixed + em.split_per_piece * S : 0.0);
     const int R = native_r(M, N, sm_count);
     const double t = 16.0 * R, blocks = std::ceil((double)M / t) * std::ceil((double)N / t);
-    const double fma_per_sm = blocks / sm_count * 256.0 * 16.0 * R * R;
-    const double nat_us = kNatFixedUs + std::ceil((double)K / NAT_KT) * (kNatSliceUs + kNatSlicePerSmFmaUs * fma_per_sm);
+    const double fma_per_sm_per_k = blocks / sm_count * 256.0 * R * R;
+    const double nat_us = kNatFixedUs + (double)K * (nat_per_k_us(R) + kNatPerFmaPerSmUs * fma_per_sm_per_k);
     return nat_us < emu_us ? EMU_MODE_FP32 : mode;
 }
 
