@@ -60,6 +60,22 @@ def config_id(name):
     return {"pet_small": 2, "pet_large": 3, "wide_l1": 4, "wide_l2": 4}[name]
 
 
+def max_over_ranks(x, world, device):
+    """The largest of every rank's x (the slowest replica sets the job's
+    time); x itself on one process."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank_step, world, step_ms):
+    """Replicas: every rank does one step's work in the (slowest) step time."""
+    return world * flops_per_rank_step / (step_ms * 1e-3) / 1e12
+
+
 def step_flops(s):
     return 2 * (2.0 * s.M * s.N * s.K)  # forward + input gradient
 
@@ -275,12 +291,9 @@ def main():
         raise RuntimeError(emu.emu_status_string(st))
     step_ms = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(K)) / K
     fwd_ms, bwd_ms = isolated_launch_ms(stream, flush, fwd, bwd, min(K, 200))
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(step_ms, world, dev)
     flops = step_flops(s)
-    value = world * flops / (step_ms * 1e-3) / 1e12
+    value = whole_job_tflops(flops, world, step_ms)
 
     peaks, peak_kind = load_peaks()
     # tensor work per effective FLOP, in BF16-rate units (TF32 runs at half rate)
@@ -294,11 +307,8 @@ def main():
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(emu, mode, s, X, Wt, b, dY, dev, stream, n=max(5, min(K, 50)))
-        if world > 1:
-            t = torch.tensor([e2e["ms"]], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e["ms"] = float(t.item())
-        e2e = {"value": world * flops / (e2e["ms"] * 1e-3) / 1e12, "unit": "TFLOPS",
+        e2e["ms"] = max_over_ranks(e2e["ms"], world, dev)
+        e2e = {"value": whole_job_tflops(flops, world, e2e["ms"]), "unit": "TFLOPS",
                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]}
 
     if rank != 0:
