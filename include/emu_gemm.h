@@ -40,7 +40,8 @@
  *     gives C = beta * C (+ bias).  beta == 0 never reads C, so C may hold NaN.
  *   - Accuracy: BF16x9 results lie within 2*K*2^-24 * (|alpha| |op(A)||op(B)|
  *     + |beta||C| + |bias|) of the exact result, elementwise; TF32x3 within
- *     4*K*2^-24 times the same.  Inputs must be finite: the split of an Inf
+ *     4*K*2^-24 times the same; EMU_MODE_FP32 within the usual bound of a
+ *     sequential FP32 sum, K*2^-24 / (1 - K*2^-24) times the same.  Inputs must be finite: the split of an Inf
  *     produces NaN components (Inf - Inf), so Inf is not propagated as IEEE
  *     arithmetic would.  BF16 components below 2^-133 are lost, so inputs
  *     with |x| < 2^-110 are represented with reduced relative precision.
@@ -122,8 +123,8 @@ emu_status_t emu_linear_fwd(emu_mode_t mode, int64_t M, int64_t N, int64_t K,
  *   The input-gradient pass of the same layer, emulated as well (blog,
  *   "TF32x3 on Ampere GPUs": forces are derivatives of the energy, so the
  *   gradient to the layer input uses the emulated arithmetic too).  All
- *   operands dense row-major.  The weight gradient is not part of the
- *   library (the blog computes it with standard FP32).
+ *   operands dense row-major.  The weight gradient has its own call,
+ *   emu_linear_bwd_weight.
  */
 emu_status_t emu_linear_bwd_input(emu_mode_t mode, int64_t M, int64_t N, int64_t K,
                                   const float *dY, const float *W, float *dX,
