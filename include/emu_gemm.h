@@ -41,7 +41,7 @@
  *   - Accuracy: BF16x9 results lie within 2*K*2^-24 * (|alpha| |op(A)||op(B)|
  *     + |beta||C| + |bias|) of the exact result, elementwise; TF32x3 within
  *     4*K*2^-24 times the same; EMU_MODE_FP32 within the usual bound of a
- *     sequential FP32 sum and its epilogue, (K+2)*2^-24 / (1 - (K+2)*2^-24)
+ *     sequential FP32 sum and its epilogue, (K+3)*2^-24 / (1 - (K+3)*2^-24)
  *     times the same.  Inputs must be finite: the split of an Inf
  *     produces NaN components (Inf - Inf), so Inf is not propagated as IEEE
  *     arithmetic would.  BF16 components below 2^-133 are lost, so inputs
