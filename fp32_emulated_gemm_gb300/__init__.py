@@ -440,7 +440,8 @@ def _autograd():
 
         def forward(self, x):
             shp = x.shape
-            packed = self._packed_weight() if self.prepack else None
+            # (native FP32 has no packed form: prepack then has nothing to do)
+            packed = self._packed_weight() if self.prepack and _mode(self.mode) != EMU_MODE_FP32 else None
             y = EmuLinearFunction.apply(x.reshape(-1, shp[-1]), self.weight, self.bias, self.mode,
                                         self.weight_grad, packed)
             return y.reshape(*shp[:-1], self.out_features)

@@ -95,3 +95,23 @@ def test_packed_calls_reject_native_mode():
     B = torch.zeros((64, 64), device="cuda")
     with pytest.raises((emu.EmuError, KeyError, ValueError)):
         emu.pack_b(B, mode="fp32")
+
+
+def test_emu_linear_module_in_native_mode():
+    """EmuLinear with mode="fp32": forward and input gradient are the native
+    kernel's (bit-identical to the oracle's SGEMM); prepack has no packed
+    form to use and is ignored."""
+    import torch
+    import fp32_emulated_gemm_gb300 as emu
+    torch.manual_seed(5)
+    layer = emu.EmuLinear(72, 40, mode="fp32", prepack=True).cuda()
+    x = torch.randn(130, 72, device="cuda", requires_grad=True)
+    y = layer(x)
+    g = torch.randn_like(y)
+    y.backward(g)
+    assert emu.emu_stream_check() == 0
+    W = layer.weight.detach().cpu().numpy()
+    b = layer.bias.detach().cpu().numpy()
+    X = x.detach().cpu().numpy()
+    _same_bits(y.detach().cpu().numpy(), oracle.sgemm_f32(oracle.Problem(X, W, transB=True, bias=b)))
+    _same_bits(x.grad.cpu().numpy(), oracle.sgemm_f32(oracle.Problem(g.cpu().numpy(), W)))
