@@ -64,9 +64,9 @@ std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-template <int MODE, int PIPE>
+template <int MODE, int PIPE, bool STAGED = false>
 cudaError_t set_smem_attr() {
-    return cudaFuncSetAttribute(emu_gemm_kernel<MODE, PIPE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(emu_gemm_kernel<MODE, PIPE, STAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 smem_bytes<MODE, PIPE>());
 }
 
@@ -139,7 +139,13 @@ emu_status_t device_info(DeviceInfo** out) {
             set_smem_attr<MODE_BF16X6, PIPE_SHORT_K_PACKED>() != cudaSuccess ||
             set_smem_attr<MODE_BF16X6, PIPE_LONG_K_PACKED>() != cudaSuccess ||
             set_smem_attr<MODE_TF32X3, PIPE_SHORT_K_PACKED>() != cudaSuccess ||
-            set_smem_attr<MODE_TF32X1, PIPE_SHORT_K_PACKED>() != cudaSuccess) {
+            set_smem_attr<MODE_TF32X1, PIPE_SHORT_K_PACKED>() != cudaSuccess ||
+            set_smem_attr<MODE_BF16X9, PIPE_SHORT_K, true>() != cudaSuccess ||
+            set_smem_attr<MODE_BF16X9, PIPE_LONG_K, true>() != cudaSuccess ||
+            set_smem_attr<MODE_BF16X9, PIPE_SHORT_K_PACKED, true>() != cudaSuccess ||
+            set_smem_attr<MODE_BF16X9, PIPE_LONG_K_PACKED, true>() != cudaSuccess ||
+            set_smem_attr<MODE_TF32X3, PIPE_SHORT_K, true>() != cudaSuccess ||
+            set_smem_attr<MODE_TF32X3, PIPE_SHORT_K_PACKED, true>() != cudaSuccess) {
             cudaGetLastError();
             return EMU_STATUS_LAUNCH_FAILED;
         }
@@ -646,11 +652,15 @@ unsigned long long wait_budget_ns() {
     return v;
 }
 
-template <int MODE, int PIPE>
+template <int MODE, int PIPE, bool STAGED = false>
 cudaError_t launch_one(cudaLaunchConfig_t cfg, const Params& p) {
     cfg.dynamicSmemBytes = smem_bytes<MODE, PIPE>();
-    return cudaLaunchKernelEx(&cfg, emu_gemm_kernel<MODE, PIPE>, p);
+    return cudaLaunchKernelEx(&cfg, emu_gemm_kernel<MODE, PIPE, STAGED>, p);
 }
+
+// Plans whose split tiles have this many pieces or more use the kernel's
+// staged reduction (BF16x9 and TF32x3; the comparators keep the register one).
+constexpr int kStagedMinPieces = 12;
 
 // The launch's own status (cudaLaunchKernelEx), so that an error left by an
 // unrelated earlier runtime call on this host thread is not reported as ours.
@@ -663,6 +673,7 @@ bool pdl_enabled() {
 }
 
 cudaError_t launch_gemm(emu_mode_t mode, int pipe, const Params& p, int clusters, cudaStream_t stream) {
+    const bool staged = (p.split_a > p.split_b ? p.split_a : p.split_b) >= kStagedMinPieces;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
     cfg.blockDim = dim3(NUM_THREADS, 1, 1);
@@ -678,7 +689,11 @@ cudaError_t launch_gemm(emu_mode_t mode, int pipe, const Params& p, int clusters
     cudaError_t e;
     switch (mode) {
         case EMU_MODE_TF32X3:
-            e = packed ? launch_one<MODE_TF32X3, PIPE_SHORT_K_PACKED>(cfg, p) : launch_one<MODE_TF32X3, PIPE_SHORT_K>(cfg, p);
+            if (staged)
+                e = packed ? launch_one<MODE_TF32X3, PIPE_SHORT_K_PACKED, true>(cfg, p)
+                           : launch_one<MODE_TF32X3, PIPE_SHORT_K, true>(cfg, p);
+            else
+                e = packed ? launch_one<MODE_TF32X3, PIPE_SHORT_K_PACKED>(cfg, p) : launch_one<MODE_TF32X3, PIPE_SHORT_K>(cfg, p);
             break;
         case EMU_MODE_TF32X1:
             e = packed ? launch_one<MODE_TF32X1, PIPE_SHORT_K_PACKED>(cfg, p) : launch_one<MODE_TF32X1, PIPE_SHORT_K>(cfg, p);
@@ -689,9 +704,16 @@ cudaError_t launch_gemm(emu_mode_t mode, int pipe, const Params& p, int clusters
                        : (long_k ? launch_one<MODE_BF16X6, PIPE_LONG_K>(cfg, p) : launch_one<MODE_BF16X6, PIPE_SHORT_K>(cfg, p));
             break;
         default:
-            e = packed ? (long_k ? launch_one<MODE_BF16X9, PIPE_LONG_K_PACKED>(cfg, p)
-                                 : launch_one<MODE_BF16X9, PIPE_SHORT_K_PACKED>(cfg, p))
-                       : (long_k ? launch_one<MODE_BF16X9, PIPE_LONG_K>(cfg, p) : launch_one<MODE_BF16X9, PIPE_SHORT_K>(cfg, p));
+            if (staged)
+                e = packed ? (long_k ? launch_one<MODE_BF16X9, PIPE_LONG_K_PACKED, true>(cfg, p)
+                                     : launch_one<MODE_BF16X9, PIPE_SHORT_K_PACKED, true>(cfg, p))
+                           : (long_k ? launch_one<MODE_BF16X9, PIPE_LONG_K, true>(cfg, p)
+                                     : launch_one<MODE_BF16X9, PIPE_SHORT_K, true>(cfg, p));
+            else
+                e = packed ? (long_k ? launch_one<MODE_BF16X9, PIPE_LONG_K_PACKED>(cfg, p)
+                                     : launch_one<MODE_BF16X9, PIPE_SHORT_K_PACKED>(cfg, p))
+                           : (long_k ? launch_one<MODE_BF16X9, PIPE_LONG_K>(cfg, p)
+                                     : launch_one<MODE_BF16X9, PIPE_SHORT_K>(cfg, p));
     }
     if (e != cudaSuccess) {
         cudaGetLastError();

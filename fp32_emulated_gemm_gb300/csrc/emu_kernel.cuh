@@ -384,7 +384,10 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int u) {
     return w;
 }
 
-template <int MODE, int PIPE>
+// STAGED: split tiles of many pieces read the other pieces' partials through
+// the output staging area (see the epilogue); a separate instantiation, so
+// that plans with few pieces keep the register-only reduction's code.
+template <int MODE, int PIPE, bool STAGED = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 emu_gemm_kernel(const __grid_constant__ Params p) {
     using C = Cfg<MODE>;
@@ -728,7 +731,56 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                 if (!published) { ok = false; break; }
                 __threadfence();
                 // the owner's own partial first, then the other pieces in
-                // increasing order, added in place (a fixed order per chunk)
+                // increasing order, added in place (a fixed order per chunk).
+                // Reads of L2 are latency-bound, so the more bytes in flight
+                // the fewer round trips: when few warps own chunks (many
+                // pieces: three or more staging blocks per owner), the owners
+                // borrow the whole output staging area
+                // (idle until the stores below) and copy several pieces'
+                // blocks into it at once with cp.async, which holds no
+                // registers while the copies fly; otherwise each owner reads
+                // one piece's block at a time into registers.
+                int n_owners = 0, my_slot0 = 0;
+                if constexpr (STAGED) {
+#pragma unroll 1
+                    for (int e2 = 0; e2 < NUM_EPI_WARPS; ++e2) {
+                        bool any = false;
+                        for (int c = 0; c < ACC / 32; ++c) any = any || (4 * e2 + c) % S == w.piece;
+                        if (any) {
+                            if (e2 < static_cast<int>(e)) ++my_slot0;
+                            ++n_owners;
+                        }
+                    }
+                }
+                constexpr int STAGED_BLOCKS = NUM_EPI_WARPS * STAGE_OUT_BYTES / 4096;  // 4 KB blocks of staging
+                const int G = STAGED && n_owners > 0 ? STAGED_BLOCKS / n_owners : 0;  // blocks per owner warp
+                if (STAGED && G >= 3) {
+                    uint8_t* slots = out_stage + static_cast<uint32_t>(my_slot0 * G) * 4096u + lane * 16u;
+#pragma unroll
+                    for (int c = 0; c < ACC / 32; ++c) {
+                        if (!owns(c)) continue;
+                        for (int qi0 = 0; qi0 < S - 1; qi0 += G) {
+                            const int n = S - 1 - qi0 < G ? S - 1 - qi0 : G;
+                            for (int t = 0; t < n; ++t) {
+                                const int qi = qi0 + t, q = qi + (qi >= w.piece ? 1 : 0);
+                                const float* src = tile_ws + static_cast<size_t>(q) * per_piece + c * 1024;
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) cp_async16(slots + t * 4096 + j * 512, src + j * 128);
+                            }
+                            cp_async_wait_all();  // each lane reads back only what it copied
+                            for (int t = 0; t < n; ++t) {
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    const float4 x = *reinterpret_cast<const float4*>(slots + t * 4096 + j * 512);
+                                    acc[32 * c + 4 * j] = __fadd_rn(acc[32 * c + 4 * j], x.x);
+                                    acc[32 * c + 4 * j + 1] = __fadd_rn(acc[32 * c + 4 * j + 1], x.y);
+                                    acc[32 * c + 4 * j + 2] = __fadd_rn(acc[32 * c + 4 * j + 2], x.z);
+                                    acc[32 * c + 4 * j + 3] = __fadd_rn(acc[32 * c + 4 * j + 3], x.w);
+                                }
+                            }
+                        }
+                    }
+                } else {
 #pragma unroll
                 for (int c = 0; c < ACC / 32; ++c) {
                     if (!owns(c)) continue;
@@ -746,6 +798,7 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                             acc[32 * c + 4 * j + 3] = __fadd_rn(acc[32 * c + 4 * j + 3], x[j].w);
                         }
                     }
+                }
                 }
                 named_bar_sync(EPI_BARRIER, NUM_EPI_WARPS * 32);  // this CTA's reads of the partials are done
                 if (e == 0 && lane == 0) {

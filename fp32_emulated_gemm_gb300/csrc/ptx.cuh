@@ -301,6 +301,17 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 16-byte asynchronous copy from global memory (L2, not L1) to shared
+// memory (the LDGSTS path: generic proxy, no registers held while in flight),
+// and waiting for all of this thread's outstanding copies.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                 :: "r"(smem_u32(smem_dst)), "l"(__cvta_generic_to_global(gsrc)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor of a K-major operand tile in the canonical
 // swizzled layout: rows of `row_bytes` (32, 64 or 128), 8-row groups packed
 // back to back (stride 8 * row_bytes), tile base aligned to the swizzle span.

@@ -106,3 +106,34 @@ def test_hybrid_plan_matches_tensor_core_model(mode):
     assert len(whole) and len(tail)
     _same_bits(Y[whole], oracle.gemm_tc(p, mode=mode, rows=whole, pieces=1))
     _same_bits(Y[tail], oracle.gemm_tc(p, mode=mode, rows=tail, pieces=plan["split_b"]))
+
+
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
+def test_many_piece_split_matches_tensor_core_model(mode, monkeypatch):
+    """16 pieces per tile: few warps own chunks, so the owners read the other
+    pieces' partials through the output staging area, several at once; the
+    sum order (owner first, then increasing piece) is unchanged."""
+    monkeypatch.setenv("EMU_SPLIT_K", "16")
+    rng = np.random.default_rng(25)
+    M, N, K = 300, 260, 2048
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    B = rng.standard_normal((K, N)).astype(np.float32)
+    rows = W.sample_rows(M, every=37, edge=2)
+    C = _gpu.gpu_sgemm(mode, A, B)
+    _same_bits(C[rows], oracle.gemm_tc(oracle.Problem(A, B), mode=mode, rows=rows, pieces=16))
+
+
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
+def test_weight_gradient_plan_matches_tensor_core_model(mode):
+    """The PET-small weight gradient with the library's own plan (4 tiles in
+    18 pieces), bit for bit against the model on sampled rows of dW."""
+    import fp32_emulated_gemm_gb300 as emu
+    s = W.PET_SMALL
+    plan = emu.emu_plan_query(s.N, s.K, s.M, 76)
+    assert plan["split_a"] >= 12
+    X, _, _, dY = W.linear_inputs(s, W.CONFIG_ID["pet_small"])
+    dW = emu.linear_bwd_weight(_gpu.to_dev(dY), _gpu.to_dev(X), mode=mode)
+    assert emu.emu_stream_check() == 0
+    rows = W.sample_rows(s.N, every=97, edge=2)
+    want = oracle.gemm_tc(oracle.Problem(dY, X, transA=True), mode=mode, rows=rows, pieces=plan["split_a"])
+    _same_bits(dW.cpu().numpy()[rows], want)
