@@ -96,3 +96,26 @@ def test_noalloc_rejects_plans_beyond_its_scratch(monkeypatch):
     assert st == NOT_SUPPORTED
     assert emu.emu_stream_check() == 0
     assert torch.all(C == 7.0)
+
+
+def test_noalloc_follows_the_performant_strategy():
+    """Under the performant strategy a small product requested in an emulated
+    mode runs in native FP32 here too: the native kernel's bits, equal to the
+    oracle's sequential SGEMM."""
+    import torch
+    import fp32_emulated_gemm_gb300 as emu
+    rng = np.random.default_rng(26)
+    M, N, K = 192, 256, 256
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    B = rng.standard_normal((K, N)).astype(np.float32)
+    Ad, Bd = _gpu.to_dev(A), _gpu.to_dev(B)
+    out = torch.full((M, N), float("nan"), device=_gpu.device())
+    with emu.strategy("performant"):
+        assert emu.emu_dispatch_query("bf16x9", M, N, K) == "fp32"
+        st = _noalloc()(emu.MODES["bf16x9"], 0, 0, M, N, K, 1.0, ctypes.c_void_p(Ad.data_ptr()), K,
+                        ctypes.c_void_p(Bd.data_ptr()), N, 0.0, ctypes.c_void_p(out.data_ptr()), N, _stream())
+    assert st == 0, emu.emu_status_string(st)
+    assert emu.emu_stream_check() == 0
+    got = out.cpu().numpy()
+    want = oracle.sgemm_f32(oracle.Problem(A, B))
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
