@@ -174,8 +174,19 @@ def cpu_baseline(shape, mode, target_s=10.0):
         r = min(X.shape[0], r * 4)
         dt = run(r)
     flops = 2 * (2.0 * r * shape.N * shape.K)
+    # the oracle's other functions on the same sample: rows per second and
+    # the full workload's time extrapolated from it
+    funcs = {}
+    for name, fn in (("gemm_f64", oracle.gemm_f64), ("sgemm_f32", oracle.sgemm_f32),
+                     ("gemm_bf16x9", oracle.gemm_bf16x9), ("gemm_tf32x3", oracle.gemm_tf32x3)):
+        t = time.perf_counter()
+        fn(oracle.Problem(X[:r], Wt, transB=True, bias=b))
+        fn(oracle.Problem(dY[:r], Wt))
+        ft = time.perf_counter() - t
+        funcs[name] = {"rows_per_s": r / ft, "full_step_s_extrapolated": ft * shape.M / r}
     return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"forward + input gradient on the first {r} of {shape.M} rows ({mode}), {dt:.2f} s"}
+            "sample": f"forward + input gradient on the first {r} of {shape.M} rows ({mode}), {dt:.2f} s",
+            "functions": funcs}
 
 
 def config_id_for_shape(shape):
