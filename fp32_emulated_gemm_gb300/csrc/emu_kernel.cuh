@@ -693,8 +693,6 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                 if (++b == NACC) { b = 0; bph ^= 1u; }
             }
             if (!ok) break;
-            const int row0 = (w.tile / p.tiles_n) * TILE_M + static_cast<int>(HALF * rank + quarter * 32u);
-            const int col0 = (w.tile % p.tiles_n) * TN + static_cast<int>(half * ACC);
             // Split tiles: a reduce-scatter over the tile's S pieces, which all
             // run at the same time (the plan keeps a tile's pieces in one wave
             // of units).  Chunk q = 4e + c (32 columns of
@@ -808,6 +806,10 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                     }
                 }
             }
+            // (the tile's origin is worked out here, not before the split-tile
+            // reduction, so that it holds no registers there)
+            const int row0 = (w.tile / p.tiles_n) * TILE_M + static_cast<int>(HALF * rank + quarter * 32u);
+            const int col0 = (w.tile % p.tiles_n) * TN + static_cast<int>(half * ACC);
             // ACC / OUT_COLS blocks of 32 rows x OUT_COLS columns: each lane stages
             // its row's sums in shared memory (rows of OUT_COLS * 4 bytes, 16-byte
             // chunks XOR-swizzled by row); the warp then reads them back as whole
