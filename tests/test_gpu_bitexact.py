@@ -137,3 +137,20 @@ def test_weight_gradient_plan_matches_tensor_core_model(mode):
     rows = W.sample_rows(s.N, every=97, edge=2)
     want = oracle.gemm_tc(oracle.Problem(dY, X, transA=True), mode=mode, rows=rows, pieces=plan["split_a"])
     _same_bits(dW.cpu().numpy()[rows], want)
+
+
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
+@pytest.mark.parametrize("pipe", ["0", "1"])
+def test_one_owner_split_matches_tensor_core_model(mode, pipe, monkeypatch):
+    """32 pieces: every piece owns exactly one 32-column chunk, so one warp per
+    CTA reduces and borrows all of the staging area (both pipeline shapes:
+    8 or 4 blocks of 4 KB)."""
+    monkeypatch.setenv("EMU_SPLIT_K", "32")
+    monkeypatch.setenv("EMU_PIPE", pipe)
+    rng = np.random.default_rng(27)
+    M, N, K = 250, 200, 4096
+    A = rng.standard_normal((M, K)).astype(np.float32)
+    B = rng.standard_normal((K, N)).astype(np.float32)
+    rows = W.sample_rows(M, every=41, edge=2)
+    C = _gpu.gpu_sgemm(mode, A, B)
+    _same_bits(C[rows], oracle.gemm_tc(oracle.Problem(A, B), mode=mode, rows=rows, pieces=32))
