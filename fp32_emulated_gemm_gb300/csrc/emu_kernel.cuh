@@ -782,18 +782,33 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
 #pragma unroll
                 for (int c = 0; c < ACC / 32; ++c) {
                     if (!owns(c)) continue;
-                    for (int q = 0; q < S; ++q) {
-                        if (q == w.piece) continue;
-                        const float* src = tile_ws + static_cast<size_t>(q) * per_piece + c * 1024;
-                        float4 x[8];
+                    // two pieces' blocks in flight at once, added in piece order
+                    for (int qi = 0; qi < S - 1; qi += 2) {
+                        const int qa = qi + (qi >= w.piece ? 1 : 0);
+                        const bool two = qi + 1 < S - 1;
+                        const int qb = qi + 1 + (qi + 1 >= w.piece ? 1 : 0);
+                        const float* sa = tile_ws + static_cast<size_t>(qa) * per_piece + c * 1024;
+                        const float* sb = tile_ws + static_cast<size_t>(two ? qb : qa) * per_piece + c * 1024;
+                        float4 x[8], y[8];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) x[j] = __ldcg(reinterpret_cast<const float4*>(src + j * 128));
+                        for (int j = 0; j < 8; ++j) x[j] = __ldcg(reinterpret_cast<const float4*>(sa + j * 128));
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) y[j] = __ldcg(reinterpret_cast<const float4*>(sb + j * 128));
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             acc[32 * c + 4 * j] = __fadd_rn(acc[32 * c + 4 * j], x[j].x);
                             acc[32 * c + 4 * j + 1] = __fadd_rn(acc[32 * c + 4 * j + 1], x[j].y);
                             acc[32 * c + 4 * j + 2] = __fadd_rn(acc[32 * c + 4 * j + 2], x[j].z);
                             acc[32 * c + 4 * j + 3] = __fadd_rn(acc[32 * c + 4 * j + 3], x[j].w);
+                        }
+                        if (two) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                acc[32 * c + 4 * j] = __fadd_rn(acc[32 * c + 4 * j], y[j].x);
+                                acc[32 * c + 4 * j + 1] = __fadd_rn(acc[32 * c + 4 * j + 1], y[j].y);
+                                acc[32 * c + 4 * j + 2] = __fadd_rn(acc[32 * c + 4 * j + 2], y[j].z);
+                                acc[32 * c + 4 * j + 3] = __fadd_rn(acc[32 * c + 4 * j + 3], y[j].w);
+                            }
                         }
                     }
                 }
