@@ -730,14 +730,14 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                 __threadfence();
                 // the owner's own partial first, then the other pieces in
                 // increasing order, added in place (a fixed order per chunk).
-                // Reads of L2 are latency-bound, so the more bytes in flight
-                // the fewer round trips: when few warps own chunks (many
-                // pieces: three or more staging blocks per owner), the owners
-                // borrow the whole output staging area
-                // (idle until the stores below) and copy several pieces'
-                // blocks into it at once with cp.async, which holds no
-                // registers while the copies fly; otherwise each owner reads
-                // one piece's block at a time into registers.
+                // The more bytes in flight, the fewer round trips to L2: in
+                // the STAGED build, when few warps own chunks (many pieces:
+                // three or more staging blocks per owner), the owners borrow
+                // the whole output staging area (idle until the stores below)
+                // and copy several pieces' blocks into it at once with
+                // cp.async, which holds no registers while the copies fly;
+                // otherwise each owner reads two pieces' blocks at a time
+                // into registers.
                 int n_owners = 0, my_slot0 = 0;
                 if constexpr (STAGED) {
 #pragma unroll 1
