@@ -115,3 +115,34 @@ def test_emu_linear_module_in_native_mode():
     X = x.detach().cpu().numpy()
     _same_bits(y.detach().cpu().numpy(), oracle.sgemm_f32(oracle.Problem(X, W, transB=True, bias=b)))
     _same_bits(x.grad.cpu().numpy(), oracle.sgemm_f32(oracle.Problem(g.cpu().numpy(), W)))
+
+
+def test_native_degenerate_and_narrow_sizes():
+    """The native mode's edge cases: M or N = 0 (no-op), K = 0 (C = beta C),
+    alpha = 0 with beta = 0 (NaN in C and the operands ignored), a linear
+    layer with K = 0 (Y = bias), and 1 x 1 x 1, single rows and columns."""
+    import torch
+    import fp32_emulated_gemm_gb300 as emu
+    fp32 = emu.MODES["fp32"]
+    dev = _gpu.device()
+    C = torch.full((4, 4), 7.0, device=dev)
+    emu.emu_sgemm(fp32, 0, 0, 0, 4, 4, 1.0, C, 4, C, 4, 0.0, C, 4)
+    emu.emu_sgemm(fp32, 0, 0, 4, 0, 4, 1.0, C, 4, C, 4, 0.0, C, 4)
+    assert emu.emu_stream_check() == 0 and torch.all(C == 7.0)
+    Cold = torch.arange(16, dtype=torch.float32, device=dev).reshape(4, 4)
+    C = Cold.clone()
+    emu.emu_sgemm(fp32, 0, 0, 4, 4, 0, 1.0, C, 4, C, 4, 2.0, C, 4)
+    assert emu.emu_stream_check() == 0 and torch.equal(C, 2 * Cold)
+    A = torch.full((4, 8), float("nan"), device=dev)
+    C = torch.full((4, 4), float("nan"), device=dev)
+    emu.emu_sgemm(fp32, 0, 0, 4, 4, 8, 0.0, A, 8, A, 8, 0.0, C, 4)
+    assert emu.emu_stream_check() == 0 and torch.all(C == 0)
+    b = torch.arange(4, dtype=torch.float32, device=dev)
+    Y = torch.full((3, 4), float("nan"), device=dev)
+    emu.emu_linear_fwd(fp32, 3, 4, 0, Y, Y, b, Y)
+    assert emu.emu_stream_check() == 0 and torch.equal(Y, b.expand(3, 4))
+    rng = np.random.default_rng(44)
+    for (M, N, K) in [(1, 1, 1), (1, 300, 64), (257, 1, 64), (130, 130, 1), (4, 4, 4)]:
+        A = rng.standard_normal((M, K)).astype(np.float32)
+        B = rng.standard_normal((K, N)).astype(np.float32)
+        _same_bits(_gpu.gpu_sgemm("fp32", A, B), oracle.sgemm_f32(oracle.Problem(A, B)))
