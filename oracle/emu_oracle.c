@@ -51,6 +51,12 @@
  *   - alpha/beta/bias: C = fmaf(alpha, acc, beta * C_old) + bias; beta == 0
  *     never reads C_old.
  *
+ * Pins: every function in this file is checked on the CPU against something
+ * other than itself (exact rational arithmetic, closed forms, hand-derived
+ * golden values, brute force on tiny inputs; tests/test_oracle_*.py), and
+ * planted mistakes in each one are caught (tests/test_oracle_mutations.py).
+ * None is unpinned.
+ *
  * Matrices are row-major.  op(A) is M x K: A[m*lda + k] when transA == 0,
  * A[k*lda + m] when transA == 1.  op(B) is K x N: B[k*ldb + n] when
  * transB == 0, B[n*ldb + k] when transB == 1.  C is M x N with leading
