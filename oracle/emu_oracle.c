@@ -499,6 +499,163 @@ ORACLE_API int oracle_gemm_tf32x1(int transA, int transB, int64_t M, int64_t N, 
 }
 
 /* ------------------------------------------------------------------------ */
+/* The emulated result with exact accumulation                               */
+/* ------------------------------------------------------------------------ */
+
+/* A fixed-point accumulator wide enough to hold any sum of up to 2^31
+ * products of two FP32 numbers without rounding: 32-bit digits (kept in
+ * int64 so that additions need no carry until the end) at weights
+ * 2^(SA_EMIN + 32 i).  The smallest product of two nonzero FP32 numbers is
+ * 2^-298 (53-bit significand in binary64: last bit 2^-350 at worst); the
+ * largest is below 2^256, and 2^31 of them below 2^287. */
+#define SA_EMIN (-384)
+#define SA_DIGITS 24
+typedef struct { int64_t d[SA_DIGITS]; } superacc;
+
+/* Add a finite binary64 value exactly (every value added here is a normal
+ * binary64 number: a product of two FP32 numbers, times a power of two). */
+static inline void sa_add(superacc *s, double x)
+{
+    uint64_t u;
+    memcpy(&u, &x, 8);
+    const int be = (int)((u >> 52) & 0x7FF);
+    if (be == 0) return;                           /* zero */
+    const uint64_t m = (u & ((UINT64_C(1) << 52) - 1)) | (UINT64_C(1) << 52);
+    const int pos = be - 1075 - SA_EMIN;           /* |x| = m 2^(SA_EMIN + pos) */
+    const int i = pos >> 5;
+    const unsigned __int128 v = (unsigned __int128)m << (pos & 31);
+    const int64_t sg = (u >> 63) ? -1 : 1;
+    s->d[i] += sg * (int64_t)(uint32_t)v;
+    s->d[i + 1] += sg * (int64_t)(uint32_t)(v >> 32);
+    s->d[i + 2] += sg * (int64_t)(uint32_t)(v >> 64);
+}
+
+/* Propagate carries: every digit but the last in [0, 2^32). */
+static void sa_carry(superacc *s)
+{
+    for (int i = 0; i < SA_DIGITS - 1; ++i) {
+        const int64_t c = (s->d[i] - (s->d[i] & 0xFFFFFFFF)) / ((int64_t)1 << 32);  /* floor division */
+        s->d[i] -= c * ((int64_t)1 << 32);
+        s->d[i + 1] += c;
+    }
+}
+
+/* The accumulator's exact value rounded once to FP32, to nearest with ties
+ * to even (overflow to infinity, gradual underflow), as an IEEE conversion
+ * of the exact value would.  It is first rounded to 53 bits "to odd" (the
+ * last bit records whether anything below it was nonzero); a rounding to
+ * odd at 53 bits followed by a rounding to nearest at 24 bits or fewer is
+ * the correctly rounded result. */
+static float sa_round_f32(superacc *s)
+{
+    sa_carry(s);
+    const int neg = s->d[SA_DIGITS - 1] < 0;
+    if (neg) {
+        for (int i = 0; i < SA_DIGITS; ++i) s->d[i] = -s->d[i];
+        sa_carry(s);
+    }
+    int top = SA_DIGITS - 1;
+    while (top >= 0 && s->d[top] == 0) --top;
+    if (top < 0) return 0.0f;
+    unsigned __int128 w = 0;
+    int sticky = 0;
+    for (int i = top; i >= top - 2; --i) w = (w << 32) | (uint32_t)(i >= 0 ? s->d[i] : 0);
+    for (int i = top - 3; i >= 0; --i) sticky |= s->d[i] != 0;
+    int e = SA_EMIN + 32 * (top - 2);              /* weight of bit 0 of w */
+    int nbits = 0;
+    for (unsigned __int128 t = w; t; t >>= 1) ++nbits;
+    if (nbits > 53) {
+        const int sh = nbits - 53;
+        sticky |= (w & ((((unsigned __int128)1) << sh) - 1)) != 0;
+        w >>= sh;
+        e += sh;
+    }
+    uint64_t t53 = (uint64_t)w;
+    if (sticky) t53 |= 1u;
+    const float f = (float)ldexp((double)t53, e);  /* the double is exact; one rounding to FP32 */
+    return neg ? -f : f;
+}
+
+/* The emulated GEMM with its accumulation made exact: the method's selected
+ * component products -- BF16x9 ([Blog] Fig. 1): the nine products
+ * 2^-8(i+j) c_i(a) c_j(b) of the scaled components; BF16x6: those of bands
+ * 0-2; TF32x3 ([Blog] Eq. 1): a_hi b_hi + a_hi b_lo + a_lo b_hi; one-pass
+ * TF32: a_hi b_hi -- each exact, summed over k with no rounding at all, the
+ * sum then rounded once to FP32 (nearest, ties to even), then the FP32
+ * epilogue.  It is the limit that "accumulated in FP32" approaches as the
+ * accumulation error vanishes, whatever its order: the reference against
+ * which the error of any FP32 accumulation of the same products is
+ * measured.  kind: 0 BF16x9, 1 BF16x6, 2 TF32x3, 3 one-pass TF32. */
+ORACLE_API int oracle_gemm_exact_sum(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                                     float alpha, const float *A, int64_t lda,
+                                     const float *B, int64_t ldb,
+                                     float beta, const float *Cold, int64_t ldc,
+                                     const float *bias, int kind,
+                                     const int64_t *rows, int64_t nrows, float *C)
+{
+    if (kind < 0 || kind > 3) return -2;
+    if (K > INT32_MAX / 9) return -2;
+    if (!rows) nrows = M;
+    float *pa = pack_opA(transA, M, K, A, lda);
+    float *pb = pack_opBt(transB, N, K, B, ldb);
+    float *sa = pa ? (float *)malloc(sizeof(float) * 3 * (size_t)(M * K > 0 ? M * K : 1)) : NULL;
+    float *sb = pb ? (float *)malloc(sizeof(float) * 3 * (size_t)(N * K > 0 ? N * K : 1)) : NULL;
+    if (!sa || !sb) { free(pa); free(pb); free(sa); free(sb); return -1; }
+    const int64_t MK = M * K, NK = N * K;
+    for (int side = 0; side < 2; ++side) {
+        const float *x = side ? pb : pa;
+        float *out = side ? sb : sa;
+        const int64_t n = side ? NK : MK;
+        for (int64_t i = 0; i < n; ++i) {
+            if (kind <= 1) {
+                split3(x[i], &out[i], &out[n + i], &out[2 * n + i]);
+            } else {
+                split2(x[i], TF32X3_HI_RN, &out[i], &out[n + i]);
+                out[2 * n + i] = 0.0f;
+            }
+        }
+    }
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t m = row_at(rows, r);
+        for (int64_t n = 0; n < N; ++n) {
+            superacc s;
+            memset(&s, 0, sizeof s);
+            for (int64_t k = 0; k < K; ++k) {
+                const double a0 = sa[m * K + k], a1 = sa[MK + m * K + k], a2 = sa[2 * MK + m * K + k];
+                const double b0 = sb[n * K + k], b1 = sb[NK + n * K + k], b2 = sb[2 * NK + n * K + k];
+                if (kind <= 1) {
+                    /* band i + j carries the scale 2^-8(i+j); every product and
+                     * scaling below is exact in binary64 */
+                    sa_add(&s, a0 * b0);
+                    sa_add(&s, a0 * b1 * 0x1p-8);
+                    sa_add(&s, a1 * b0 * 0x1p-8);
+                    sa_add(&s, a0 * b2 * 0x1p-16);
+                    sa_add(&s, a1 * b1 * 0x1p-16);
+                    sa_add(&s, a2 * b0 * 0x1p-16);
+                    if (kind == 0) {
+                        sa_add(&s, a1 * b2 * 0x1p-24);
+                        sa_add(&s, a2 * b1 * 0x1p-24);
+                        sa_add(&s, a2 * b2 * 0x1p-32);
+                    }
+                } else {
+                    /* a0, b0 = hi; a1, b1 = lo */
+                    sa_add(&s, a0 * b0);
+                    if (kind == 2) {
+                        sa_add(&s, a0 * b1);
+                        sa_add(&s, a1 * b0);
+                    }
+                }
+            }
+            const float acc = sa_round_f32(&s);
+            C[r * N + n] = epilogue_f32(acc, alpha, beta, Cold + m * ldc + n, bias ? bias + n : NULL);
+        }
+    }
+    free(pa); free(pb); free(sa); free(sb);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Tensor-core accumulation model                                            */
 /* ------------------------------------------------------------------------ */
 

@@ -11,6 +11,7 @@ import numpy as np
 import oracle
 from tests import _bits
 from tests import test_oracle_gemm as g
+from tests import test_oracle_exact as x
 from tests import test_oracle_split as s
 from tests import test_oracle_tc as tc
 
@@ -57,6 +58,18 @@ def run_pins():
     for mode in ("bf16x9", "tf32x3"):
         tc.test_model_within_the_stated_error_bound(mode)
     tc.test_split_pieces_are_reduced_owner_first()
+    tc.test_issue_order_is_smallest_band_first()
+    tc.test_each_32_deep_stage_starts_from_zero_and_is_promoted_to_nearest()
+    # exact-accumulation reference pins
+    for tA, tB in x.TRANS:
+        x.test_bf16x9_exact_sum_is_the_correctly_rounded_dot_product(tA, tB)
+        x.test_tf32x3_exact_sum_closed_form(tA, tB)
+    x.test_bf16x6_and_tf32x1_exact_sum_closed_forms()
+    x.test_exact_cancellation_of_huge_terms()
+    x.test_rounding_is_nearest_even_once()
+    x.test_subnormal_and_overflowing_results()
+    x.test_epilogue_and_row_sampling()
+    x.test_sequential_fp32_accumulation_stays_near_the_exact_sum()
 
 
 if __name__ == "__main__":

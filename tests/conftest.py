@@ -26,3 +26,20 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    # every GPU-vs-oracle comparison's metrics (normwise error and bound,
+    # elementwise excesses against the exact-accumulation and the sequential
+    # oracle results), one JSON line each, when EMU_PARITY_REPORT names a file
+    path = os.environ.get("EMU_PARITY_REPORT")
+    if not path:
+        return
+    try:
+        from tests import _gpu
+    except Exception:
+        return
+    import json
+    with open(path, "a") as f:
+        for r in _gpu.REPORT:
+            f.write(json.dumps(r) + "\n")

@@ -1,6 +1,12 @@
 """GPU parity at the full sizes of the PET-like, wide-model and stress
 workloads, in the launch configuration the benchmark times, checked on
-deterministic row samples the oracle can evaluate row by row."""
+deterministic row samples the oracle can evaluate row by row.
+
+Besides the tolerances of _gpu.compare, BF16x9 must meet or beat native FP32
+against the float64 reference ("Unlocking Tensor Core performance for
+machine-learning interatomic potentials", "Limitations and decision
+criteria"): its normwise error may not exceed that of the oracle's native
+FP32 SGEMM (one sequential fmaf chain per output) on the same rows."""
 import numpy as np
 import pytest
 
@@ -12,7 +18,16 @@ pytestmark = pytest.mark.gpu
 MODES = ["bf16x9", "tf32x3"]
 
 
-def _linear_pair(mode, shape, config, rows):
+def _no_worse_than_native(mode, res, p, rows):
+    """BF16x9: normwise error <= the native FP32 SGEMM's on the same rows."""
+    C64, D = oracle.gemm_f64(p, rows), oracle.absdenom_f64(p, rows)
+    e32 = oracle.normwise_error(oracle.sgemm_f32(p, rows), C64, D)
+    res["native_fp32_normwise"] = e32
+    if mode == "bf16x9":
+        assert res["normwise"] <= e32, (res["normwise"], e32)
+
+
+def _linear_pair(mode, shape, config, rows, label):
     import fp32_emulated_gemm_gb300 as emu
     X, Wt, b, dY = W.linear_inputs(shape, config)
     Y = emu.linear_fwd(_gpu.to_dev(X), _gpu.to_dev(Wt), _gpu.to_dev(b), mode=mode)
@@ -20,8 +35,11 @@ def _linear_pair(mode, shape, config, rows):
     assert emu.emu_stream_check() == 0
     Yh, dXh = Y.cpu().numpy(), dX.cpu().numpy()
     del Y, dX
-    r1 = _gpu.compare(mode, Yh, oracle.Problem(X, Wt, transB=True, bias=b), rows)
-    r2 = _gpu.compare(mode, dXh, oracle.Problem(dY, Wt), rows)
+    pf, pb = oracle.Problem(X, Wt, transB=True, bias=b), oracle.Problem(dY, Wt)
+    r1 = _gpu.compare(mode, Yh, pf, rows, label=f"{label} forward")
+    _no_worse_than_native(mode, r1, pf, rows)
+    r2 = _gpu.compare(mode, dXh, pb, rows, label=f"{label} input gradient")
+    _no_worse_than_native(mode, r2, pb, rows)
     return r1, r2
 
 
@@ -31,7 +49,7 @@ def test_wide_model_layers(mode, layer):
     """M=6144; K=1024 N=4096 and K=4096 N=1024; forward and input gradient."""
     shape = W.WIDE_L1 if layer == "wide_l1" else W.WIDE_L2
     rows = W.sample_rows(shape.M, every=128, edge=64)
-    _linear_pair(mode, shape, W.CONFIG_ID["wide"], rows)
+    _linear_pair(mode, shape, W.CONFIG_ID["wide"], rows, layer)
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -39,16 +57,25 @@ def test_pet_large(mode):
     """M=552960, K=256, N=1024 forward and input gradient (17,280 atoms x 32)."""
     shape = W.PET_LARGE
     rows = W.sample_rows(shape.M, every=2048, edge=128)
-    _linear_pair(mode, shape, W.CONFIG_ID["pet_large"], rows)
+    _linear_pair(mode, shape, W.CONFIG_ID["pet_large"], rows, "pet_large")
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_pet_small_no_worse_than_native(mode):
+    """PET-small forward and input gradient on a row sample: the tolerances,
+    and BF16x9 no less accurate than native FP32."""
+    shape = W.PET_SMALL
+    rows = W.sample_rows(shape.M, every=32, edge=64)
+    _linear_pair(mode, shape, W.CONFIG_ID["pet_small"], rows, "pet_small")
 
 
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("n", list(W.STRESS_SIZES))
 def test_stress_sweep(mode, n):
     """Square GEMMs, magnitudes 2^U[-20,20], 1% zeros/subnormals/huge values:
-    the normwise bound against float64 holds; BF16x9 is also compared with
-    the oracle's native FP32 SGEMM error (reported, and required to be no
-    worse than 4x it at these sizes)."""
+    the normwise bound against float64 and the elementwise bars hold on the
+    sampled rows; the ratio of BF16x9's normwise error to the native FP32
+    SGEMM's is recorded (the report) and must not exceed 1."""
     A, B = W.stress_inputs(n)
     if n <= 1024:
         rows = np.arange(n)
@@ -58,8 +85,5 @@ def test_stress_sweep(mode, n):
         rows = np.array([0, 1, n // 3, n // 2, n - 2, n - 1], dtype=np.int64)
     C = _gpu.gpu_sgemm(mode, A, B)
     p = oracle.Problem(A, B)
-    res = _gpu.compare(mode, C, p, rows, elementwise=False)
-    if mode == "bf16x9":
-        C64, D = oracle.gemm_f64(p, rows), oracle.absdenom_f64(p, rows)
-        e32 = oracle.normwise_error(oracle.sgemm_f32(p, rows), C64, D)
-        assert res["normwise"] <= 4 * max(e32, 2.0 ** -24), (res["normwise"], e32)
+    res = _gpu.compare(mode, C, p, rows, label=f"stress n={n}")
+    _no_worse_than_native(mode, res, p, rows)

@@ -55,6 +55,19 @@ MUTANTS = {
                              "if (round_mode == 7 && fabs((double)f) > fabs(v))"),
     "tc_floors_terms": ("S += (int64_t)trunc(ldexp((double)a[i] * (double)b[i], -q));",
                         "S += (int64_t)floor(ldexp((double)a[i] * (double)b[i], -q));"),
+    "tc_issue_largest_first": ("pi9[9] = {2, 1, 2, 0, 1, 2, 0, 1, 0}, pj9[9] = {2, 2, 1, 2, 1, 0, 1, 0, 0}",
+                               "pi9[9] = {0, 1, 0, 2, 1, 0, 2, 1, 2}, pj9[9] = {0, 0, 1, 0, 1, 2, 1, 2, 2}"),
+    "tc_stage_doubled": ("    if (block < 1 || block > 64 || stage_k < block",
+                         "    stage_k *= 2;\n    if (block < 1 || block > 64 || stage_k < block"),
+    # exact-accumulation reference
+    "exact_band3_product_dropped": ("sa_add(&s, a2 * b1 * 0x1p-24);", ";"),
+    "exact_band1_scale": ("sa_add(&s, a0 * b1 * 0x1p-8);", "sa_add(&s, a0 * b1 * 0x1p-7);"),
+    "exact_tf32_lo_hi_dropped": ("sa_add(&s, a0 * b1);\n                        sa_add(&s, a1 * b0);",
+                                 "sa_add(&s, a0 * b1);"),
+    "exact_no_sticky_bit": ("if (sticky) t53 |= 1u;", ";"),
+    "exact_sign_ignored": ("const int64_t sg = (u >> 63) ? -1 : 1;", "const int64_t sg = 1;"),
+    "exact_carry_truncates": ("const int64_t c = (s->d[i] - (s->d[i] & 0xFFFFFFFF)) / ((int64_t)1 << 32);",
+                              "const int64_t c = s->d[i] / ((int64_t)1 << 32);"),
     "tc_owner_last": ("acc = part[owner];\n                for (int q = 0; q < pieces; ++q)\n                    if (q != owner) acc = acc + part[q];",
                       "acc = part[owner == 0 ? 1 : 0];\n                for (int q = 0; q < pieces; ++q)\n                    if (q != (owner == 0 ? 1 : 0)) acc = acc + part[q];"),
 }

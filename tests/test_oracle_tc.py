@@ -135,3 +135,41 @@ def test_split_pieces_are_reduced_owner_first():
                 if q != owner:
                     acc = np.float32(acc + parts[q][m, n])
             assert got[m, n] == acc
+
+
+def test_issue_order_is_smallest_band_first():
+    """The products of a stage go into the accumulator smallest band first,
+    the order the north-star reading of [Blog] Fig. 1 gives ("ordered
+    smallest band first").  Worked by hand for a = b = 1 + 2^-8 + 2^-16,
+    whose components in natural magnitude are 1, 2^-8 and 2^-16 (K = 1, so
+    each product is one block FMA with the accumulator):
+      smallest first, the accumulator holds 2^-32, then 2^-24 + 2^-32,
+      2^-23 + 2^-32, then the band-2 products make 3 2^-16 + 2^-23 + 2^-32;
+      adding 2^-8 (alignment exponent -8, FP32 result rounded toward zero)
+      drops 2^-32; the second 2^-8 and finally 1 keep everything else:
+      1 + 2^-7 + 3 2^-16 + 2^-23 (the correctly rounded a*b);
+      largest first, the two band-3 products of 2^-24 arrive at an
+      accumulator near 1 whose FP32 rounding toward zero drops each of them:
+      1 + 2^-7 + 3 2^-16."""
+    a = np.float32(1.0 + 2.0 ** -8 + 2.0 ** -16)
+    C = oracle.gemm_tc(oracle.Problem(np.array([[a]]), np.array([[a]])), mode="bf16x9")
+    assert C[0, 0] == np.float32(1.0 + 2.0 ** -7 + 3 * 2.0 ** -16 + 2.0 ** -23)
+    assert C[0, 0] != np.float32(1.0 + 2.0 ** -7 + 3 * 2.0 ** -16)
+
+
+def test_each_32_deep_stage_starts_from_zero_and_is_promoted_to_nearest():
+    """Stages of 32 k-values, each summed from zero and added into the FP32
+    result with rounding to nearest.  Worked by hand for K = 64, operands
+    exact in BF16 (one component each): a_0 b_0 = 1 and three products
+    2^-12 2^-13 = 2^-25 at k = 32, 33, 34 (all other products zero).  Stage
+    one gives 1; stage two sums its three products exactly to 3 2^-25, and
+    1 + 3 2^-25 rounded to nearest is 1 + 2^-23.  (One 64-deep stage would
+    add the 2^-25 products to an accumulator holding 1: kept within the
+    2-bit alignment window, 1 + 3 2^-25, then rounded toward zero to 1.)"""
+    A = np.zeros((1, 64), np.float32)
+    B = np.zeros((64, 1), np.float32)
+    A[0, 0] = B[0, 0] = 1.0
+    A[0, 32:35] = 2.0 ** -12
+    B[32:35, 0] = 2.0 ** -13
+    C = oracle.gemm_tc(oracle.Problem(A, B), mode="bf16x9")
+    assert C[0, 0] == np.float32(1.0 + 2.0 ** -23)

@@ -7,9 +7,10 @@ error mid-run.  For them the library offers emu_sgemm_noalloc, whose split-K
 scratch is a fixed 64 MiB device array inside the library.
 
 These tests call it through the C ABI and compare it with emu_sgemm (same
-kernel, same plan) within the tolerance the other GPU tests use, on two calls
-in a row (the shared array keeps the previous call's contents).  This file is
-collected last on purpose.
+kernel, same plan, so the same bits: asserted bit for bit, which also covers
+the tolerance the other GPU tests use), on two calls in a row (the shared
+array keeps the previous call's contents).  This file is collected last on
+purpose.
 """
 import ctypes
 
@@ -69,6 +70,7 @@ def test_noalloc_matches_emu_sgemm_on_two_calls(mode, case):
         assert emu.emu_stream_check() == 0
         got = out.cpu().numpy()
         assert np.all(np.isfinite(got)), f"call {call}: non-finite output"
+        assert np.array_equal(got.view(np.uint32), ref_h.view(np.uint32)), f"call {call}: bits differ from emu_sgemm"
         ex = oracle.elementwise_excess(got, ref_h)
         assert ex <= 1.0, f"call {call}: differs from emu_sgemm beyond 1e-5 relative (excess {ex:.3f})"
     # and against the float64 oracle on a row sample, like the other tests
