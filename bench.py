@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-comparators", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads and modes reported under extras.workloads")
     ap.add_argument("--rows", type=int, default=0,
                     help="replace the workload's M (token rows) by this many, for profiler captures of a "
                          "smaller case of the same kernel; the JSON line names the changed workload")
@@ -153,10 +155,96 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def host_info():
+    """The CPU this runs on: model name (x86 'model name', Arm implementer /
+    part ids) and the cores this process may use."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            txt = f.read()
+        for key in ("model name", "Model", "CPU part"):
+            for line in txt.splitlines():
+                if line.lower().startswith(key.lower()):
+                    model = (model + ", " if model else "") + line.split(":", 1)[1].strip()
+                    break
+            if model and key == "model name":
+                break
+    except OSError:
+        pass
+    import platform
+    usable = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"model": model or platform.processor() or platform.machine(), "machine": platform.machine(),
+            "nproc": usable, "cpu_count": os.cpu_count()}
+
+
+_ONE_CORE_CODE = r"""
+import json, sys, time
+sys.path.insert(0, %r)
+import oracle
+from fp32_emulated_gemm_gb300 import workloads as W
+s = W.PET_SMALL
+X, Wt, b, dY = W.linear_inputs(s, W.CONFIG_ID["pet_small"], rows=%d)
+out = {"threads": oracle.num_threads()}
+for mode in ("bf16x9", "tf32x3"):
+    t = time.perf_counter()
+    oracle.gemm_emulated(oracle.Problem(X, Wt, transB=True, bias=b), mode)
+    oracle.gemm_emulated(oracle.Problem(dY, Wt), mode)
+    out[mode] = time.perf_counter() - t
+print(json.dumps(out))
+"""
+
+
+def cpu_protocol():
+    """The oracle's timing protocol on this host: the PET-small step (forward
+    + input gradient) and the tiny problem in full on all cores; the wide
+    layers on the deterministic row sample of their parity tests (every
+    128th row plus the first and last 64), extrapolated to all rows and
+    labelled so; and the PET-small
+    step on a 256-row sample on one core (a child process with
+    OMP_NUM_THREADS=1).  Seconds per step, both modes."""
+    import oracle
+    from fp32_emulated_gemm_gb300 import workloads as W
+    res = {"host": host_info(), "threads_all": oracle.num_threads()}
+    A, B, Cold = W.tiny_inputs()
+    for mode in ("bf16x9", "tf32x3"):
+        t = time.perf_counter()
+        oracle.gemm_emulated(oracle.Problem(A, B, beta=1.0, C_old=Cold), mode)
+        res.setdefault("tiny_full_s", {})[mode] = time.perf_counter() - t
+    s = W.PET_SMALL
+    X, Wt, b, dY = W.linear_inputs(s, W.CONFIG_ID["pet_small"])
+    for mode in ("bf16x9", "tf32x3"):
+        t = time.perf_counter()
+        oracle.gemm_emulated(oracle.Problem(X, Wt, transB=True, bias=b), mode)
+        oracle.gemm_emulated(oracle.Problem(dY, Wt), mode)
+        dt = time.perf_counter() - t
+        res.setdefault("pet_small_full_step_s", {})[mode] = dt
+    for lname, shape in (("wide_l1", W.WIDE_L1), ("wide_l2", W.WIDE_L2)):
+        rows = W.sample_rows(shape.M, every=128, edge=64)
+        X, Wt, b, dY = W.linear_inputs(shape, W.CONFIG_ID["wide"])
+        for mode in ("bf16x9", "tf32x3"):
+            t = time.perf_counter()
+            oracle.gemm_emulated(oracle.Problem(X, Wt, transB=True, bias=b), mode, rows)
+            oracle.gemm_emulated(oracle.Problem(dY, Wt), mode, rows)
+            dt = time.perf_counter() - t
+            res.setdefault(f"{lname}_sampled", {})[mode] = {
+                "rows": int(rows.size), "of": shape.M, "sample_s": dt,
+                "full_step_s_extrapolated": dt * shape.M / rows.size}
+    r1 = 256
+    try:
+        out = subprocess.run([sys.executable, "-c", _ONE_CORE_CODE % (ROOT, r1)], capture_output=True,
+                             text=True, timeout=300, env=dict(os.environ, OMP_NUM_THREADS="1"))
+        one = json.loads(out.stdout.strip().splitlines()[-1])
+        res["one_core"] = {"threads": one["threads"], "sample": f"PET-small step on the first {r1} of {s.M} rows",
+                           **{m: {"sample_s": one[m], "full_step_s_extrapolated": one[m] * s.M / r1}
+                              for m in ("bf16x9", "tf32x3")}}
+    except Exception as exc:  # reported, not fatal
+        res["one_core"] = {"unavailable": str(exc)[:200]}
+    return res
+
+
 def cpu_baseline(shape, mode, target_s=10.0):
     """The CPU oracle on a bounded row sample of the same step (forward + input
     gradient on the first r rows), timed on this host's cores."""
-    import numpy as np
     import oracle
     from fp32_emulated_gemm_gb300 import workloads as W
     oracle.build()
@@ -186,7 +274,7 @@ def cpu_baseline(shape, mode, target_s=10.0):
         funcs[name] = {"rows_per_s": r / ft, "full_step_s_extrapolated": ft * shape.M / r}
     return {"value": flops / dt / 1e12, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"forward + input gradient on the first {r} of {shape.M} rows ({mode}), {dt:.2f} s",
-            "functions": funcs}
+            "functions": funcs, "protocol": cpu_protocol()}
 
 
 def config_id_for_shape(shape):
@@ -307,12 +395,14 @@ def main():
     value = whole_job_tflops(flops, world, step_ms)
 
     peaks, peak_kind = load_peaks()
-    # tensor work per effective FLOP, in BF16-rate units (TF32 runs at half rate)
-    tensor_units = {"bf16x9": 9.0, "bf16x6": 6.0, "tf32x3": 6.0, "tf32x1": 2.0}[args.mode]
-    peak = peaks["bf16_tflops"] / tensor_units
+    peak = peaks["bf16_tflops"] / TENSOR_UNITS[args.mode]
     # dominant kernel: the emulated-GEMM kernel (both launches of a step);
-    # algorithmic work per launch = 2 M N K effective FLOPs
-    achieved = (flops / 2) / ((step_ms / 2) * 1e-3) / 1e12
+    # algorithmic work per launch = 2 M N K effective FLOPs, over the average
+    # duration of a launch timed alone (events on both sides of it, no
+    # overlap with its neighbour); the step-based figure, which credits the
+    # overlap of the two launches, is reported beside it
+    achieved = (flops / 2) / (0.5 * (fwd_ms + bwd_ms) * 1e-3) / 1e12
+    achieved_step = (flops / 2) / ((step_ms / 2) * 1e-3) / 1e12
     traffic = load_traffic(args)
 
     e2e = None
@@ -331,10 +421,12 @@ def main():
         "config": workload_config(args, s),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_kind} bf16 dense burst / {tensor_units:g}",
+                     "peak_source": f"{peak_kind} bf16 dense burst / {TENSOR_UNITS[args.mode]:g}",
                      "kernel": f"emu_gemm_kernel<{args.mode}>",
-                     "launch_ms": step_ms / 2,
-                     "isolated_fwd_ms": fwd_ms, "isolated_bwd_ms": bwd_ms},
+                     "launch_ms": 0.5 * (fwd_ms + bwd_ms),
+                     "isolated_fwd_ms": fwd_ms, "isolated_bwd_ms": bwd_ms,
+                     "achieved_step": achieved_step, "frac_step": achieved_step / peak,
+                     "step_launch_ms": step_ms / 2},
         "gpu_launches": launches_per_step(emu, args.mode, s) * K,
         "wall_s_timed_region": wall,
     }
@@ -347,7 +439,90 @@ def main():
     if not args.no_comparators:
         line["comparators"] = cublas_comparators(s)
         line["extras"] = extra_passes(emu, mode, s, Xd, dYd, flush, stream, fwd, bwd, peak)
+        if not args.no_workloads and args.rows == 0:
+            line["extras"]["workloads"] = other_workloads(emu, args, peaks, peak_kind, dev, stream, flush)
     print(json.dumps(line), flush=True)
+
+
+# tensor work per effective FLOP, in BF16-rate units (TF32 runs at half rate)
+TENSOR_UNITS = {"bf16x9": 9.0, "bf16x6": 6.0, "tf32x3": 6.0, "tf32x1": 2.0}
+
+# Beside the headline (PET-small, BF16x9), the same measurement on the other
+# PET-shaped workloads and in the other mode.
+OTHER_WORKLOADS = [("pet_small", "tf32x3"), ("pet_large", "bf16x9"), ("pet_large", "tf32x3"),
+                   ("wide_l1", "bf16x9"), ("wide_l1", "tf32x3"), ("wide_l2", "bf16x9"), ("wide_l2", "tf32x3")]
+
+
+def device_linear_inputs(s, config, dev):
+    """The workload's inputs drawn on the device (seeded torch generators,
+    one per tensor, seed 100 config + tensor id; X ~ N(0,1), W ~ N(0,1/K),
+    b ~ N(0,0.01), dY ~ N(0,1)): the large workloads' gigabytes need no host
+    draw or copy.  Same distributions as workloads.linear_inputs."""
+    import torch
+
+    def normal(shape, std, tensor_id):
+        g = torch.Generator(device=dev)
+        g.manual_seed(100 * config + tensor_id)
+        return torch.randn(shape, generator=g, device=dev).mul_(std)
+
+    return (normal((s.M, s.K), 1.0, 0), normal((s.N, s.K), s.K ** -0.5, 1), normal((s.N,), 0.1, 2),
+            normal((s.M, s.N), 1.0, 3))
+
+
+def other_workloads(emu, args, peaks, peak_kind, dev, stream, flush):
+    """Each (workload, mode) of OTHER_WORKLOADS timed like the headline: the
+    step (forward + input gradient between one event pair, L2 flushed before
+    it) and each launch alone; effective TFLOPS and the fraction of the
+    measured BF16 peak over the mode's tensor work, both from the step and
+    from the launches timed alone (the kernel's own duration, no overlap)."""
+    import torch
+    out = {}
+    sp = stream.cuda_stream
+    for name, mode_name in OTHER_WORKLOADS:
+        s = shape_of(name)
+        mode = emu.MODES[mode_name]
+        X, Wt, b, dY = device_linear_inputs(s, config_id(name), dev)
+        Y = torch.empty((s.M, s.N), device=dev)
+        dX = torch.empty((s.M, s.K), device=dev)
+
+        def fwd():
+            emu.emu_linear_fwd(mode, s.M, s.N, s.K, X, Wt, b, Y, sp)
+
+        def bwd():
+            emu.emu_linear_bwd_input(mode, s.M, s.N, s.K, dY, Wt, dX, sp)
+
+        flops = step_flops(s)
+        K = 20 if s.M > 100000 else 100
+        for _ in range(3):
+            flush.fill_(1.0)
+            fwd()
+            bwd()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        for i in range(K):
+            flush.fill_(float(i & 7))
+            ev[i][0].record(stream)
+            fwd()
+            bwd()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        st = emu.emu_stream_check(sp)
+        if st != 0:
+            raise RuntimeError(f"{name} {mode_name}: {emu.emu_status_string(st)}")
+        step_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+        f_ms, b_ms = isolated_launch_ms(stream, flush, fwd, bwd, K)
+        peak = peaks["bf16_tflops"] / TENSOR_UNITS[mode_name]
+        iso = (flops / 2) / (0.5 * (f_ms + b_ms) * 1e-3) / 1e12
+        val = flops / (step_ms * 1e-3) / 1e12
+        out[f"{name}_{mode_name}"] = {
+            "workload": f"{name}: M={s.M} K={s.K} N={s.N}, forward + input gradient", "mode": mode_name,
+            "steps": K, "ms_per_step": step_ms, "value": val, "unit": "TFLOPS", "frac_step": val / peak,
+            "isolated_fwd_ms": f_ms, "isolated_bwd_ms": b_ms, "achieved_isolated": iso, "frac_isolated": iso / peak,
+            "peak": peak, "peak_source": f"{peak_kind} bf16 dense burst / {TENSOR_UNITS[mode_name]:g}",
+            "gpu_launches_per_step": launches_per_step(emu, mode_name, s),
+            "l2": "flushed before every step (256 MB write)", "inputs": "drawn on the device, seeded"}
+        del X, Wt, b, dY, Y, dX
+        torch.cuda.empty_cache()
+    return out
 
 
 def launches_per_step(emu, mode, s):

@@ -23,6 +23,7 @@ __all__ = [
     "EmuError",
     "emu_sgemm", "emu_linear_fwd", "emu_linear_bwd_input", "emu_linear_bwd_weight", "emu_status_string",
     "emu_stream_check", "emu_split_dump", "emu_plan_query", "emu_version",
+    "emu_selftest_wait_timeout", "emu_selftest_split_timeout", "emu_shutdown", "emu_debug_fail_allocations",
     "emu_set_strategy", "emu_get_strategy", "emu_dispatch_query", "strategy",
     "emu_pack_bytes", "emu_pack_b", "emu_sgemm_packed_b", "emu_linear_fwd_packed", "emu_linear_bwd_input_packed",
     "pack_b", "sgemm_packed", "PackedWeight", "pack_weight", "linear_fwd_packed", "linear_bwd_input_packed",
@@ -101,9 +102,13 @@ def load():
         L.emu_get_strategy.restype = i32
         L.emu_dispatch_query.argtypes = [i32, i64, i64, i64, i32, ctypes.POINTER(i32)]
         L.emu_dispatch_query.restype = i32
+        L.emu_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P]
+        L.emu_selftest_split_timeout.argtypes = [ctypes.c_uint64, i64, P]
+        L.emu_shutdown.argtypes = []
+        L.emu_debug_fail_allocations.argtypes = [i32]
         for name in ("emu_sgemm", "emu_linear_fwd", "emu_linear_bwd_input", "emu_linear_bwd_weight",
-                     "emu_stream_check",
-                     "emu_split_dump", "emu_version"):
+                     "emu_stream_check", "emu_split_dump", "emu_version", "emu_selftest_wait_timeout",
+                     "emu_selftest_split_timeout", "emu_shutdown", "emu_debug_fail_allocations"):
             getattr(L, name).restype = i32
         _lib = L
         return L
@@ -153,6 +158,24 @@ def emu_status_string(status: int) -> str:
 
 def emu_stream_check(stream=None) -> int:
     return int(load().emu_stream_check(ctypes.c_void_p(_stream(stream))))
+
+
+def emu_selftest_wait_timeout(budget_ns, stream=None):
+    _check(load().emu_selftest_wait_timeout(int(budget_ns), ctypes.c_void_p(_stream(stream))),
+           "emu_selftest_wait_timeout")
+
+
+def emu_selftest_split_timeout(budget_ns, tiles, stream=None):
+    _check(load().emu_selftest_split_timeout(int(budget_ns), int(tiles), ctypes.c_void_p(_stream(stream))),
+           "emu_selftest_split_timeout")
+
+
+def emu_shutdown():
+    _check(load().emu_shutdown(), "emu_shutdown")
+
+
+def emu_debug_fail_allocations(n):
+    _check(load().emu_debug_fail_allocations(int(n)), "emu_debug_fail_allocations")
 
 
 def emu_split_dump(mode, R, Kc, X, ldx, mn_major, out, stream=None):

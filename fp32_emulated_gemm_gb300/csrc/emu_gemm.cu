@@ -43,21 +43,35 @@ struct DeviceInfo {
     int max_clusters[2] = {0, 0};  // co-resident CTA pairs per mode (all pipeline shapes)
 };
 
-// Split-K workspace: partial tiles plus per-tile counters, owned by the
-// library, one per (device, stream) so that calls on different streams never
-// share it.  Grown on demand, kept until the process exits.
+// Split-K workspace: partial tiles plus per-tile arrival counters, owned by
+// the library, one per (device, stream) so that calls on different streams
+// never share it.  Grown on demand, kept until emu_shutdown() or the end of
+// the process.  `epoch` numbers the launches that use its counters.
 struct Workspace {
     int device = -1;
     cudaStream_t stream = nullptr;
     float* partials = nullptr;
     size_t partial_floats = 0;
-    int* counters = nullptr;
+    unsigned long long* counters = nullptr;
     size_t num_counters = 0;
+    unsigned long long epoch = 0;
     void* packed = nullptr;   // op(B) split ahead of a product (automatic pre-split)
     size_t packed_bytes = 0;
 };
-constexpr int kMaxWorkspaces = 64;
+constexpr int kMaxWorkspaces = 64;   // (device, stream) pairs with a workspace at once
 Workspace g_ws[kMaxWorkspaces];
+
+// Test hook (emu_debug_fail_allocations): the next n device allocations the
+// library attempts fail as if the allocator were out of memory.
+std::atomic<int> g_fail_allocs{0};
+
+cudaError_t lib_malloc_async(void** ptr, size_t bytes, cudaStream_t stream) {
+    int n = g_fail_allocs.load();
+    while (n > 0) {
+        if (g_fail_allocs.compare_exchange_weak(n, n - 1)) return cudaErrorMemoryAllocation;
+    }
+    return cudaMallocAsync(ptr, bytes, stream);
+}
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
@@ -451,23 +465,31 @@ emu_status_t check_error_flag(bool clear) {
     return flag ? EMU_STATUS_DEVICE_TIMEOUT : EMU_STATUS_SUCCESS;
 }
 
-// The workspace for (current device, stream), at least `floats` partial
-// floats and `counters` zeroed counters.  Allocation happens only when the
-// cached one is too small; the counters are zeroed on the stream.
-emu_status_t workspace_for(int dev, cudaStream_t stream, size_t floats, size_t counters, Workspace** out) {
-    std::lock_guard<std::mutex> lock(g_mutex);
-    Workspace* w = nullptr;
+// The slot of (device, stream) in the workspace table, taken on first use;
+// nullptr when all kMaxWorkspaces slots hold other pairs.  Caller holds g_mutex.
+Workspace* workspace_slot(int dev, cudaStream_t stream) {
     for (auto& c : g_ws)
-        if (c.device == dev && c.stream == stream) { w = &c; break; }
-    if (!w)
-        for (auto& c : g_ws)
-            if (c.device < 0) { w = &c; w->device = dev; w->stream = stream; break; }
+        if (c.device == dev && c.stream == stream) return &c;
+    for (auto& c : g_ws)
+        if (c.device < 0) { c.device = dev; c.stream = stream; return &c; }
+    return nullptr;
+}
+
+// The workspace for (current device, stream) with at least `floats` partial
+// floats and `counters` arrival counters, and a new epoch for the launch
+// about to use it.  Allocation happens only when the cached one is too
+// small; new counters are zeroed on the stream (epoch 0, which no launch
+// uses).
+emu_status_t workspace_for(int dev, cudaStream_t stream, size_t floats, size_t counters, Workspace** out,
+                           unsigned long long* epoch) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    Workspace* w = workspace_slot(dev, stream);
     if (!w) return EMU_STATUS_ALLOC_FAILED;
     if (w->partial_floats < floats) {
         if (w->partials && cudaFreeAsync(w->partials, stream) != cudaSuccess) cudaGetLastError();
         w->partials = nullptr;
         w->partial_floats = 0;
-        if (cudaMallocAsync(reinterpret_cast<void**>(&w->partials), floats * sizeof(float), stream) != cudaSuccess) {
+        if (lib_malloc_async(reinterpret_cast<void**>(&w->partials), floats * sizeof(float), stream) != cudaSuccess) {
             cudaGetLastError();
             return EMU_STATUS_ALLOC_FAILED;
         }
@@ -477,33 +499,30 @@ emu_status_t workspace_for(int dev, cudaStream_t stream, size_t floats, size_t c
         if (w->counters && cudaFreeAsync(w->counters, stream) != cudaSuccess) cudaGetLastError();
         w->counters = nullptr;
         w->num_counters = 0;
-        if (cudaMallocAsync(reinterpret_cast<void**>(&w->counters), counters * sizeof(int), stream) != cudaSuccess ||
-            cudaMemsetAsync(w->counters, 0, counters * sizeof(int), stream) != cudaSuccess) {
+        const size_t bytes = counters * sizeof(unsigned long long);
+        if (lib_malloc_async(reinterpret_cast<void**>(&w->counters), bytes, stream) != cudaSuccess ||
+            cudaMemsetAsync(w->counters, 0, bytes, stream) != cudaSuccess) {
             cudaGetLastError();
             return EMU_STATUS_ALLOC_FAILED;
         }
         w->num_counters = counters;
     }
+    *epoch = ++w->epoch;
     *out = w;
     return EMU_STATUS_SUCCESS;
 }
 
 // A buffer for an automatically pre-split op(B), per (device, stream), grown
-// on demand with cudaMallocAsync and kept.
+// on demand and kept.
 emu_status_t packed_buffer_for(int dev, cudaStream_t stream, size_t bytes, void** out) {
     std::lock_guard<std::mutex> lock(g_mutex);
-    Workspace* w = nullptr;
-    for (auto& c : g_ws)
-        if (c.device == dev && c.stream == stream) { w = &c; break; }
-    if (!w)
-        for (auto& c : g_ws)
-            if (c.device < 0) { w = &c; w->device = dev; w->stream = stream; break; }
+    Workspace* w = workspace_slot(dev, stream);
     if (!w) return EMU_STATUS_ALLOC_FAILED;
     if (w->packed_bytes < bytes) {
         if (w->packed && cudaFreeAsync(w->packed, stream) != cudaSuccess) cudaGetLastError();
         w->packed = nullptr;
         w->packed_bytes = 0;
-        if (cudaMallocAsync(&w->packed, bytes, stream) != cudaSuccess) {
+        if (lib_malloc_async(&w->packed, bytes, stream) != cudaSuccess) {
             cudaGetLastError();
             return EMU_STATUS_ALLOC_FAILED;
         }
@@ -790,26 +809,27 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
                    ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
     }
     Plan plan = make_plan(M, N, K, pairs);
+    int devid = 0;
+    cudaGetDevice(&devid);
+    // Everything that can fail -- the library's buffers, the tensor maps --
+    // comes before the first launch, so that a call that returns an error
+    // has enqueued nothing.
     static const bool autopack = env_int("EMU_AUTOPACK", 1) != 0;
+    void* autopack_buf = nullptr;
     if (!packed_b && autopack && (mode == EMU_MODE_TF32X3 || mode == EMU_MODE_TF32X1) &&
         plan.tiles_m >= kAutoPackMinTileRows && (size_t)packed_bytes(mode, N, K) <= kAutoPackMaxBytes) {
-        int devid = 0;
-        cudaGetDevice(&devid);
-        void* buf = nullptr;
-        st = packed_buffer_for(devid, stream, (size_t)packed_bytes(mode, N, K), &buf);
+        st = packed_buffer_for(devid, stream, (size_t)packed_bytes(mode, N, K), &autopack_buf);
         if (st != EMU_STATUS_SUCCESS) return st;
-        if (launch_pack(mode, N, K, B, ldb, !b_mn, buf, dev->sm_count, stream) != cudaSuccess)
-            return EMU_STATUS_LAUNCH_FAILED;
-        packed_b = buf;
     }
-    if (packed_b) plan.pipe = plan.pipe == PIPE_LONG_K ? PIPE_LONG_K_PACKED : PIPE_SHORT_K_PACKED;
+    const void* b_packed = packed_b ? packed_b : autopack_buf;
+    if (b_packed) plan.pipe = plan.pipe == PIPE_LONG_K ? PIPE_LONG_K_PACKED : PIPE_SHORT_K_PACKED;
     Params p{};
     if (!encode_operand(&p.tmA, A, a_mn, M, K, lda, HALF) ||
-        !(packed_b ? encode_packed(&p.tmB, packed_b, mode, N, K)
+        !(b_packed ? encode_packed(&p.tmB, b_packed, mode, N, K)
                    : encode_operand(&p.tmB, B, b_mn, N, K, ldb, (uint32_t)plan.tn / 2)))
         return EMU_STATUS_LAUNCH_FAILED;
     p.M = (int)M; p.N = (int)N; p.K = (int)K;
-    p.a_mn_major = a_mn; p.b_mn_major = packed_b ? 0 : b_mn;
+    p.a_mn_major = a_mn; p.b_mn_major = b_packed ? 0 : b_mn;
     p.tiles_m = plan.tiles_m;
     p.tiles_n = plan.tiles_n;
     p.num_tiles = plan.num_tiles;
@@ -821,15 +841,15 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
     p.bias = bias;
     p.wait_budget_ns = wait_budget_ns();
     if (plan.slots > 0) {
-        int devid = 0;
-        cudaGetDevice(&devid);
         Workspace* w = nullptr;
         const size_t floats = (size_t)plan.slots * TILE_M * plan.tn;
-        st = workspace_for(devid, stream, floats, (size_t)p.num_tiles * 4, &w);
+        st = workspace_for(devid, stream, floats, (size_t)p.num_tiles * 2, &w, &p.epoch);
         if (st != EMU_STATUS_SUCCESS) return st;
         p.workspace = w->partials;
         p.counters = w->counters;
     }
+    if (autopack_buf && launch_pack(mode, N, K, B, ldb, !b_mn, autopack_buf, dev->sm_count, stream) != cudaSuccess)
+        return EMU_STATUS_LAUNCH_FAILED;
     const int clusters = plan.clusters;
     if (log_enabled())
         std::fprintf(stderr, "[emu] %s M=%lld N=%lld K=%lld a_mn=%d b_mn=%d pipe=%d tile=256x%d tiles=%dx%d "
@@ -896,6 +916,21 @@ __global__ void wait_timeout_selftest_kernel(unsigned long long budget_ns) {
     }
     __syncwarp();
     mbar_wait_warp(&bar, 0, &abort_flag, budget_ns, 7);
+}
+
+// Self-test of the split-K counters after a timeout: for one launch epoch,
+// every counter gets one arrival (as if one piece of every split tile had
+// published), then thread 0 waits for a second arrival that never comes, as
+// a split piece whose partner pieces are lost would; its wait gives up after
+// the budget.  The counts it leaves behind belong to that epoch.
+__global__ void split_timeout_selftest_kernel(unsigned long long* counters, int n, unsigned long long epoch,
+                                              unsigned long long budget_ns) {
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) abort_flag = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) epoch_arrive(&counters[i], epoch);
+    __syncthreads();
+    if (threadIdx.x == 0) wait_epoch_count(&counters[0], epoch, 2u, &abort_flag, budget_ns, 8);
 }
 
 }  // namespace
@@ -1041,6 +1076,51 @@ emu_status_t emu_selftest_wait_timeout(uint64_t budget_ns, emu_stream_t stream) 
     return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
 }
 
+emu_status_t emu_selftest_split_timeout(uint64_t budget_ns, int64_t tiles, emu_stream_t stream) {
+    if (budget_ns == 0 || budget_ns > 10000000000ull || tiles < 1 || tiles > (int64_t(1) << 24))
+        return EMU_STATUS_INVALID_VALUE;
+    DeviceInfo* dev = nullptr;
+    emu_status_t st = device_info(&dev);
+    if (st != EMU_STATUS_SUCCESS) return st;
+    int devid = 0;
+    cudaGetDevice(&devid);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    Workspace* w = nullptr;
+    unsigned long long epoch = 0;
+    st = workspace_for(devid, s, 0, (size_t)tiles * 2, &w, &epoch);
+    if (st != EMU_STATUS_SUCCESS) return st;
+    cudaGetLastError();
+    split_timeout_selftest_kernel<<<1, 256, 0, s>>>(w->counters, (int)(tiles * 2), epoch, budget_ns);
+    return cudaGetLastError() == cudaSuccess ? EMU_STATUS_SUCCESS : EMU_STATUS_LAUNCH_FAILED;
+}
+
+emu_status_t emu_shutdown(void) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int current = 0;
+    const bool have_current = cudaGetDevice(&current) == cudaSuccess;
+    emu_status_t result = EMU_STATUS_SUCCESS;
+    for (auto& w : g_ws) {
+        if (w.device < 0) continue;
+        if (cudaSetDevice(w.device) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+            cudaGetLastError();
+            result = EMU_STATUS_LAUNCH_FAILED;
+        }
+        // after the device synchronisation nothing uses these buffers
+        if (w.partials && cudaFree(w.partials) != cudaSuccess) { cudaGetLastError(); result = EMU_STATUS_LAUNCH_FAILED; }
+        if (w.counters && cudaFree(w.counters) != cudaSuccess) { cudaGetLastError(); result = EMU_STATUS_LAUNCH_FAILED; }
+        if (w.packed && cudaFree(w.packed) != cudaSuccess) { cudaGetLastError(); result = EMU_STATUS_LAUNCH_FAILED; }
+        w = Workspace{};
+    }
+    if (have_current && cudaSetDevice(current) != cudaSuccess) cudaGetLastError();
+    return result;
+}
+
+emu_status_t emu_debug_fail_allocations(int n) {
+    if (n < 0) return EMU_STATUS_INVALID_VALUE;
+    g_fail_allocs.store(n);
+    return EMU_STATUS_SUCCESS;
+}
+
 emu_status_t emu_plan_query(int64_t M, int64_t N, int64_t K, int pairs, int64_t* out, int n) {
     if (M <= 0 || N <= 0 || K <= 0 || pairs < 1 || !out || n < EMU_PLAN_FIELDS) return EMU_STATUS_INVALID_VALUE;
     if (M > INT32_MAX - 256 || N > INT32_MAX - 256 || K > INT32_MAX - 256) return EMU_STATUS_NOT_SUPPORTED;
@@ -1091,8 +1171,9 @@ namespace {
 // address, never the name's host-side value.
 std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[kMaxDevices] = {};
+unsigned long long g_noalloc_epoch[kMaxDevices] = {};
 
-emu_status_t noalloc_scratch(void** out) {
+emu_status_t noalloc_scratch(void** out, unsigned long long* epoch) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         cudaGetLastError();
@@ -1108,6 +1189,7 @@ emu_status_t noalloc_scratch(void** out) {
         g_noalloc_ptr[dev] = ptr;
     }
     *out = g_noalloc_ptr[dev];
+    *epoch = ++g_noalloc_epoch[dev];
     return EMU_STATUS_SUCCESS;
 }
 
@@ -1131,7 +1213,8 @@ emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, 
     emu_status_t st = device_info(&dev);
     if (st != EMU_STATUS_SUCCESS) return st;
     void* scratch = nullptr;
-    st = noalloc_scratch(&scratch);
+    unsigned long long epoch = 0;
+    st = noalloc_scratch(&scratch, &epoch);
     if (st != EMU_STATUS_SUCCESS) return st;
 
     if (!gemm) {
@@ -1171,10 +1254,11 @@ emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, 
         // partial tiles first, then the counters
         const size_t partial_bytes = (size_t)plan.slots * TILE_M * plan.tn * sizeof(float);
         const size_t counter_off = (partial_bytes + 255) & ~size_t(255);
-        const size_t counter_bytes = (size_t)p.num_tiles * 4 * sizeof(int);
+        const size_t counter_bytes = (size_t)p.num_tiles * 2 * sizeof(unsigned long long);
         if (counter_off + counter_bytes > kNoAllocScratchBytes) return EMU_STATUS_NOT_SUPPORTED;
         p.workspace = reinterpret_cast<float*>(scratch);
-        p.counters = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(scratch) + counter_off);
+        p.counters = reinterpret_cast<unsigned long long*>(reinterpret_cast<unsigned char*>(scratch) + counter_off);
+        p.epoch = epoch;
         // the array keeps the previous call's contents: the counters must start at zero
         if (cudaMemsetAsync(p.counters, 0, counter_bytes, stream) != cudaSuccess) {
             cudaGetLastError();

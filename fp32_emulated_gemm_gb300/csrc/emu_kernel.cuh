@@ -36,8 +36,10 @@
 // cut into S pieces processed by different pairs at the same time.  The
 // pieces reduce-scatter through a workspace: each publishes the parts of its
 // partial tile that the others own, and sums and stores its own part, adding
-// the S partials in the fixed order 0..S-1 -- the result does not depend on
-// timing.
+// the S partials in a fixed order (the owner's first, then the others by
+// piece index) -- the result does not depend on timing.  The pieces count
+// their arrivals on epoch-tagged counters (one new epoch per launch), so no
+// count left by an earlier launch can be taken for this one's.
 #pragma once
 
 #include <cstdint>
@@ -208,7 +210,8 @@ struct Params {
     long long ldc;
     const float* bias;   // may be null
     float* workspace;    // split tiles: S partial tiles of 256 x TN each (thread-major)
-    int* counters;       // split tiles: 4 per tile (published, finished per CTA half), zero between launches
+    unsigned long long* counters;  // split tiles: 2 per tile (pieces arrived, per CTA half), epoch-tagged
+    unsigned long long epoch;      // this launch's epoch on the counters (> 0, new for every launch)
     unsigned long long wait_budget_ns;
 };
 
@@ -718,10 +721,10 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                                make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
                 __threadfence();
                 named_bar_sync(EPI_BARRIER, NUM_EPI_WARPS * 32);
-                int* ctr = p.counters + (static_cast<size_t>(w.tile) * 2 + rank) * 2;  // published, finished
+                unsigned long long* ctr = p.counters + static_cast<size_t>(w.tile) * 2 + rank;
                 if (e == 0 && lane == 0) {
-                    atomicAdd(&ctr[0], 1);
-                    *last_flag = wait_count_geq(&ctr[0], S, abort_flag, budget, 6) ? 1 : 0;
+                    epoch_arrive(ctr, p.epoch);
+                    *last_flag = wait_epoch_count(ctr, p.epoch, static_cast<unsigned>(S), abort_flag, budget, 6) ? 1 : 0;
                 }
                 named_bar_sync(EPI_BARRIER, NUM_EPI_WARPS * 32);
                 const int published = *last_flag;
@@ -813,13 +816,9 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                     }
                 }
                 }
-                named_bar_sync(EPI_BARRIER, NUM_EPI_WARPS * 32);  // this CTA's reads of the partials are done
-                if (e == 0 && lane == 0) {
-                    if (atomicAdd(&ctr[1], 1) == S - 1) {  // the tile's last reader: ready for the next launch
-                        atomicExch(&ctr[0], 0);
-                        atomicExch(&ctr[1], 0);
-                    }
-                }
+                // the staged reads may use other warps' staging blocks: all
+                // done before any warp stages its output below
+                named_bar_sync(EPI_BARRIER, NUM_EPI_WARPS * 32);
             }
             // (the tile's origin is worked out here, not before the split-tile
             // reduction, so that it holds no registers there)

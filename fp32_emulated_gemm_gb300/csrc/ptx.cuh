@@ -124,16 +124,40 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
-// Single-thread wait until the global counter reaches `target` (acquire at
-// GPU scope, so that the writes the other CTAs released before incrementing
-// it are visible), bounded like the barrier waits.
-__device__ __forceinline__ bool wait_count_geq(const int* ctr, int target, volatile int* abort,
-                                               uint64_t budget_ns, unsigned role) {
+// Split-K arrival counters.  A counter is one 64-bit word: the epoch of the
+// launch that last arrived on it (bits 8..63) and how many pieces of that
+// launch have arrived (bits 0..7).  Every launch that uses a workspace gets a
+// new epoch from the host, so a count left by an earlier launch (one that
+// gave up on a wait before every piece arrived, say) belongs to another epoch
+// and never counts toward this launch's total; the counters need no reset
+// between launches.
+__device__ __forceinline__ unsigned long long epoch_word(unsigned long long epoch, unsigned count) {
+    return (epoch << 8) | count;
+}
+
+// Arrive once on `ctr` for `epoch` (relaxed: the caller's __threadfence and
+// barrier order the data it publishes before this).
+__device__ __forceinline__ void epoch_arrive(unsigned long long* ctr, unsigned long long epoch) {
+    unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(ctr);
+    for (;;) {
+        const unsigned long long want = (cur >> 8) == epoch ? cur + 1 : epoch_word(epoch, 1);
+        const unsigned long long prev = atomicCAS(ctr, cur, want);
+        if (prev == cur) return;
+        cur = prev;
+    }
+}
+
+// Single-thread wait until `target` pieces of `epoch` have arrived on `ctr`
+// (acquire at GPU scope, so that the writes the other CTAs released before
+// arriving are visible), bounded like the barrier waits.
+__device__ __forceinline__ bool wait_epoch_count(const unsigned long long* ctr, unsigned long long epoch,
+                                                 unsigned target, volatile int* abort, uint64_t budget_ns,
+                                                 unsigned role) {
     uint64_t t0 = 0;
     for (uint32_t i = 0;; ++i) {
-        int v;
-        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-        if (v >= target) return true;
+        unsigned long long v;
+        asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+        if ((v >> 8) == epoch && (v & 0xFFu) >= target) return true;
         if ((i & 7u) == 7u) {
             if (*abort) return false;
             const uint64_t now = globaltimer_ns();

@@ -25,11 +25,14 @@
  *   - Pointers: caller-owned DEVICE memory of the current CUDA device.  The
  *     library keeps no caller pointer after the call returns and never frees
  *     caller memory.  Its only device allocations are a split-K workspace
- *     (partial tiles for problems with few tiles) and, for the TF32 modes, a
- *     buffer for op(B) split ahead of the product (when op(A) spans four or
- *     more 256-row tiles; EMU_AUTOPACK=0 turns that off), made with
- *     cudaMallocAsync on first need per (device, stream) and kept until the
- *     process exits; emu_sgemm_noalloc never allocates.
+ *     (partial tiles and arrival counters for problems with few tiles) and,
+ *     for the TF32 modes, a buffer for op(B) split ahead of the product (when
+ *     op(A) spans four or more 256-row tiles; EMU_AUTOPACK=0 turns that off),
+ *     made with cudaMallocAsync on first need per (device, stream) and kept
+ *     until emu_shutdown() or the end of the process; emu_sgemm_noalloc never
+ *     allocates.  The library tracks at most 64 (device, stream) pairs with
+ *     such buffers at once: a call that would need a 65th returns
+ *     EMU_STATUS_ALLOC_FAILED (emu_shutdown() releases all of them).
  *   - Alignment (TMA): A and B must start on a 16-byte boundary and lda, ldb
  *     must be multiples of 4 elements; C the same (ldc multiple of 4).
  *     Violations return EMU_STATUS_NOT_SUPPORTED.
@@ -47,9 +50,11 @@
  *     arithmetic would.  BF16 components below 2^-133 are lost, so inputs
  *     with |x| < 2^-110 are represented with reduced relative precision.
  *   - Errors: no exception crosses the ABI.  A kernel whose internal waits
- *     time out records a device-side flag instead of hanging; it is reported
- *     as EMU_STATUS_DEVICE_TIMEOUT by emu_stream_check() (or by the next call
- *     on any stream).
+ *     time out records a device-side flag instead of hanging and returns; it
+ *     is reported as EMU_STATUS_DEVICE_TIMEOUT by the next emu_stream_check()
+ *     on the device (the GEMM calls themselves do not read it).  A timed-out
+ *     launch's output is incomplete; later launches are unaffected (the
+ *     split-K arrival counters are tagged per launch).
  *   - Thread safety: all entry points may be called concurrently from
  *     several host threads.
  */
@@ -86,8 +91,10 @@ typedef enum {
     EMU_STATUS_SUCCESS = 0,
     EMU_STATUS_INVALID_VALUE = 1,   /* negative size, ld too small, NULL with non-zero size, bad enum */
     EMU_STATUS_NOT_SUPPORTED = 2,   /* pointer or leading dimension not aligned for TMA; size too large */
-    EMU_STATUS_ARCH_MISMATCH = 3,   /* current device is not compute capability 10.x (sm_100 family) */
-    EMU_STATUS_ALLOC_FAILED = 4,    /* the split-K workspace could not be allocated */
+    EMU_STATUS_ARCH_MISMATCH = 3,   /* current device is not compute capability 10.3 (the library holds
+                                       sm_103a code only) */
+    EMU_STATUS_ALLOC_FAILED = 4,    /* a library buffer (split-K workspace, pre-split op(B)) could not be
+                                       allocated, or the 64 (device, stream) slots are taken */
     EMU_STATUS_LAUNCH_FAILED = 5,   /* a CUDA call failed (no device, launch error, TMA encode error) */
     EMU_STATUS_DEVICE_TIMEOUT = 6   /* a kernel gave up on an internal wait and returned early */
 } emu_status_t;
@@ -235,8 +242,8 @@ emu_status_t emu_split_dump(emu_mode_t mode, int64_t R, int64_t Kc, const float 
  *     use no scratch and are never rejected for size.
  *   - Allocation: none (no cudaMalloc/cudaFree, no allocating library
  *     routine).  The call enqueues one cudaMemsetAsync of the counters (the
- *     array keeps the previous call's contents; the counters must start at
- *     zero) and the kernel.
+ *     array keeps the previous call's contents, and the counters are cleared
+ *     on every call) and the kernel.
  *   - First call per device: looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make this first call
  *     before any stream capture.
@@ -261,6 +268,43 @@ emu_status_t emu_sgemm_noalloc(emu_mode_t mode, emu_op_t transA, emu_op_t transB
  * EMU_STATUS_DEVICE_TIMEOUT and clears the flag.  No fault, trap or hang.
  */
 emu_status_t emu_selftest_wait_timeout(uint64_t budget_ns, emu_stream_t stream);
+
+/*
+ * emu_selftest_split_timeout -- diagnostic for the split-K counters after a
+ * device timeout: takes the split-K workspace of (current device, `stream`)
+ * (allocating counters for `tiles` tiles if it has fewer) and a launch epoch,
+ * as a split launch would, and launches one block that arrives once on every
+ * counter, as if one piece of every split tile had published, and then waits,
+ * through the kernels' bounded wait, for a second arrival that never comes.
+ * After budget_ns nanoseconds (0 < budget_ns <= 10 s) the wait gives up; the
+ * next emu_stream_check() on this stream reports EMU_STATUS_DEVICE_TIMEOUT.
+ * The arrivals it leaves behind belong to its own epoch, so a later split
+ * launch on the stream is unaffected.  1 <= tiles <= 2^24, else
+ * INVALID_VALUE.  No fault, trap or hang.
+ */
+emu_status_t emu_selftest_split_timeout(uint64_t budget_ns, int64_t tiles, emu_stream_t stream);
+
+/*
+ * emu_shutdown -- release the library's cached device buffers (split-K
+ * workspaces, pre-split op(B) buffers) on every device that has them: each
+ * such device is synchronised (cudaDeviceSynchronize) first, then the buffers
+ * are freed and the (device, stream) slots cleared.  Later calls allocate
+ * again on first need.  The current device is left as it was.  Returns
+ * EMU_STATUS_LAUNCH_FAILED if a synchronisation or free failed (the slots
+ * are cleared anyway).  Not to be called while another host thread is
+ * inside a library call.  emu_sgemm_noalloc's fixed array is not freed (it
+ * lives as long as the library is loaded).
+ */
+emu_status_t emu_shutdown(void);
+
+/*
+ * emu_debug_fail_allocations -- test hook: the next n device allocations the
+ * library attempts (cudaMallocAsync of its workspace or pre-split buffers)
+ * fail as if the device were out of memory, so that the calls needing them
+ * return EMU_STATUS_ALLOC_FAILED having enqueued nothing.  n = 0 ends it.
+ * INVALID_VALUE for n < 0.  Process-wide.
+ */
+emu_status_t emu_debug_fail_allocations(int n);
 
 /*
  * emu_plan_query -- diagnostic, host only (no GPU, no CUDA call): the launch

@@ -131,3 +131,17 @@ def test_strategy_and_dispatch_are_host_decisions(lib):
     with pytest.raises(emu.EmuError):
         emu.emu_dispatch_query("bf16x9", 0, 4, 4)
     assert emu.emu_pack_bytes("fp32", 64, 64) == -1
+
+
+def test_failure_hooks_check_arguments_on_the_host(lib):
+    """The diagnostic and test-hook entry points validate their arguments
+    before touching a device; emu_shutdown with nothing cached is a no-op."""
+    L = emu.load()
+    z = ctypes.c_void_p(0)
+    assert L.emu_debug_fail_allocations(-1) == 1
+    assert L.emu_debug_fail_allocations(0) == 0
+    assert L.emu_selftest_split_timeout(0, 4, z) == 1                  # zero budget
+    assert L.emu_selftest_split_timeout(11_000_000_000, 4, z) == 1     # above 10 s
+    assert L.emu_selftest_split_timeout(1_000_000, 0, z) == 1          # no tiles
+    assert L.emu_selftest_wait_timeout(0, z) == 1
+    assert L.emu_shutdown() == 0
