@@ -139,8 +139,8 @@ def test_split_pieces_are_reduced_owner_first():
 
 def test_issue_order_is_smallest_band_first():
     """The products of a stage go into the accumulator smallest band first,
-    the order the north-star reading of [Blog] Fig. 1 gives ("ordered
-    smallest band first").  Worked by hand for a = b = 1 + 2^-8 + 2^-16,
+    the order this library reads into [Blog] Fig. 1's band accumulation
+    (bands 4, 3, 2, 1, 0).  Worked by hand for a = b = 1 + 2^-8 + 2^-16,
     whose components in natural magnitude are 1, 2^-8 and 2^-16 (K = 1, so
     each product is one block FMA with the accumulator):
       smallest first, the accumulator holds 2^-32, then 2^-24 + 2^-32,
