@@ -95,6 +95,8 @@ def load():
             getattr(L, name).restype = i32
         L.emu_plan_query.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64), i32]
         L.emu_plan_query.restype = i32
+        L.emu_plan_bounds.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64), i32]
+        L.emu_plan_bounds.restype = i32
         L.emu_version.argtypes = []
         L.emu_set_strategy.argtypes = [i32]
         L.emu_set_strategy.restype = i32
@@ -210,7 +212,7 @@ def emu_linear_bwd_input_packed(mode, M, N, K, dY, Wt_packed, dX, stream=None):
 
 
 PLAN_FIELDS = ("pipe", "tile_n", "tiles_m", "tiles_n", "k_stages", "tiles_a", "split_a", "split_b",
-               "units", "pairs", "slots", "cost_x100")
+               "units", "pairs", "slots", "cost_x100", "chain")
 
 
 def emu_plan_query(M, N, K, pairs) -> dict:
@@ -218,6 +220,14 @@ def emu_plan_query(M, N, K, pairs) -> dict:
     out = (ctypes.c_int64 * len(PLAN_FIELDS))()
     _check(load().emu_plan_query(int(M), int(N), int(K), int(pairs), out, len(PLAN_FIELDS)), "emu_plan_query")
     return dict(zip(PLAN_FIELDS, (int(v) for v in out)))
+
+
+def emu_plan_bounds(M, N, K, pairs) -> list:
+    """The run bounds of the chained plan emu_plan_query describes (host
+    only; see the header)."""
+    out = (ctypes.c_int64 * (int(pairs) + 1))()
+    _check(load().emu_plan_bounds(int(M), int(N), int(K), int(pairs), out, int(pairs) + 1), "emu_plan_bounds")
+    return [int(v) for v in out]
 
 
 def emu_version() -> int:

@@ -547,9 +547,11 @@ struct Plan {
     int tiles_m, tiles_n, num_tiles, k_stages;
     int tiles_a, split_a, split_b;  // see Params
     int num_units;
+    int chain;      // 1: chained plan (see emu_kernel.cuh); tiles_a = all tiles, whole
     int clusters;   // CTA pairs launched
     long long slots;  // workspace partial tiles (0: no split tile)
     double cost;      // predicted time in pipeline stages (see below)
+    long long chain_bound[kMaxChainPairs + 1];  // chained plans: the pairs' stage runs
 };
 
 // Long k-loops per work unit favour three component stages; short ones the
@@ -568,15 +570,118 @@ int env_int(const char* name, int dflt) {
     return v ? std::atoi(v) : dflt;
 }
 
+// Chained plans (T >= pairs tiles of KS stages; the U = T KS stages taken
+// tile by tile, pair c runs [bound[c], bound[c + 1])).  What a pair's run
+// costs, in pipeline stages (measured on GB300 with globaltimer stamps of the
+// PET-small forward pass): its stages; about 2 more for every unit before the
+// last, whose output stores (or published running sum) the next unit's first
+// two stages hide only in part; about 2 more when the last unit is a short
+// tail (2 stages or fewer) right after a whole tile, because the tail's
+// starting-sum loads queue behind that tile's stores.  Every run covers at
+// least one tile end or start (a run strictly inside one tile would cut it
+// twice).
+constexpr double kChainDrainStages = 2.0, kChainShortTailStages = 2.0;
+constexpr int kChainSlack = 2;  // each bound within this many stages of the even cut c U / pairs
+double chain_run_cost(long long s, long long e, int KS) {
+    if (e <= s) return -1.0;
+    const long long t0 = s / KS, t1 = (e - 1) / KS;
+    const long long units = t1 - t0 + 1, lo = s - t0 * KS, hi = e - t1 * KS;
+    if (units == 1 && lo > 0 && hi < KS) return -1.0;
+    double c = (double)(e - s) + kChainDrainStages * (double)(units - 1);
+    if (hi < KS && units >= 2 && (units >= 3 || lo == 0) && hi <= 2) c += kChainShortTailStages;
+    return c;
+}
+
+struct ChainPlan {
+    double cost;
+    int units, cuts;
+    long long bound[kMaxChainPairs + 1];
+};
+
+// The bounds that minimise the slowest pair's cost (then the total), each
+// within kChainSlack stages of the even cut: a bottleneck shortest path over
+// the candidate bounds, O(pairs (2 kChainSlack + 1)^2).  False when no valid
+// set exists.
+bool chain_bounds_optimised(long long U, int KS, int pairs, ChainPlan* out) {
+    constexpr int W = 2 * kChainSlack + 1;
+    long long cand[kMaxChainPairs + 1][W];
+    int ncand[kMaxChainPairs + 1];
+    double best_max[kMaxChainPairs + 1][W], best_sum[kMaxChainPairs + 1][W];
+    int prev[kMaxChainPairs + 1][W];
+    for (int c = 0; c <= pairs; ++c) {
+        ncand[c] = 0;
+        if (c == 0 || c == pairs) { cand[c][0] = c == 0 ? 0 : U; ncand[c] = 1; continue; }
+        const long long even = (long long)c * U / pairs;
+        for (int d = -kChainSlack; d <= kChainSlack; ++d) {
+            const long long v = even + d;
+            if (v >= 1 && v <= U - 1) cand[c][ncand[c]++] = v;
+        }
+    }
+    best_max[0][0] = 0.0; best_sum[0][0] = 0.0; prev[0][0] = -1;
+    for (int c = 1; c <= pairs; ++c) {
+        for (int i = 0; i < ncand[c]; ++i) {
+            best_max[c][i] = -1.0;
+            for (int j = 0; j < ncand[c - 1]; ++j) {
+                if (best_max[c - 1][j] < 0.0) continue;
+                const double rc = chain_run_cost(cand[c - 1][j], cand[c][i], KS);
+                if (rc < 0.0) continue;
+                const double mx = best_max[c - 1][j] > rc ? best_max[c - 1][j] : rc;
+                const double sm = best_sum[c - 1][j] + rc;
+                if (best_max[c][i] < 0.0 || mx < best_max[c][i] - 1e-9 ||
+                    (mx < best_max[c][i] + 1e-9 && sm < best_sum[c][i] - 1e-9)) {
+                    best_max[c][i] = mx; best_sum[c][i] = sm; prev[c][i] = j;
+                }
+            }
+        }
+    }
+    if (best_max[pairs][0] < 0.0) return false;
+    out->cost = best_max[pairs][0];
+    for (int c = pairs, i = 0; c >= 0; --c) {
+        out->bound[c] = cand[c][i];
+        if (c > 0) i = prev[c][i];
+    }
+    return true;
+}
+
+// The even cuts c U / pairs, without optimisation (a diagnostic choice).
+bool chain_bounds_even(long long U, int KS, int pairs, ChainPlan* out) {
+    out->cost = 0.0;
+    for (int c = 0; c <= pairs; ++c) out->bound[c] = (long long)c * U / pairs;
+    for (int c = 0; c < pairs; ++c) {
+        const double rc = chain_run_cost(out->bound[c], out->bound[c + 1], KS);
+        if (rc < 0.0) return false;
+        out->cost = rc > out->cost ? rc : out->cost;
+    }
+    return true;
+}
+
+bool chain_plan(long long T, int KS, int pairs, bool even_cuts, ChainPlan* out) {
+    if (pairs < 1 || pairs > kMaxChainPairs || T < pairs) return false;
+    const long long U = T * KS;
+    if (!(even_cuts ? chain_bounds_even(U, KS, pairs, out) : chain_bounds_optimised(U, KS, pairs, out)))
+        return false;
+    out->units = 0; out->cuts = 0;
+    for (int c = 0; c < pairs; ++c) {
+        out->units += (int)((out->bound[c + 1] - 1) / KS - out->bound[c] / KS + 1);
+        if (c > 0 && out->bound[c] % KS != 0) ++out->cuts;
+    }
+    return true;
+}
+
 // Candidate plans (a split tile's S pieces wait for one another, so they
 // must run in the same wave of units: S is at most the number of pairs, and
 // at most 32, the 32-column chunks of a CTA's half-tile):
 //   uniform: every tile in S pieces; with more than one wave the pairs in
 //     use are a multiple of S, so that waves hold whole tiles;
 //   hybrid: W full waves of whole tiles on all pairs, then the remaining
-//     tiles (fewer than the pairs) in S pieces, one more wave at most.
+//     tiles (fewer than the pairs) in S pieces, one more wave at most;
+//   chained: at least as many tiles as pairs, every pair one run of stages
+//     (chain_plan), a tile cut at a run boundary finished by the pair whose
+//     run ends there.
 // EMU_SPLIT_K (uniform S), EMU_SPLIT_TAIL (hybrid with that S for the
-// remaining tiles, where a hybrid plan exists) and EMU_PIPE (0 short-k,
+// remaining tiles, where a hybrid plan exists), EMU_CHAIN (0: never chained;
+// 1: chained wherever it is possible; 2: the same with the even cuts
+// c U / pairs instead of the optimised bounds) and EMU_PIPE (0 short-k,
 // 1 long-k) override the choice, for diagnostics and tuning.
 Plan make_plan(int64_t M, int64_t N, int64_t K, int pairs) {
     Plan plan{};
@@ -603,8 +708,9 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int pairs) {
     const int force_tail = env_int("EMU_SPLIT_TAIL", 0);
     const int s_max = KS < 32 ? KS : 32;
     const long long W0 = T / pairs, tail0 = T - W0 * pairs;
-    if (force_split < 1 && force_tail >= 2 && W0 >= 1 && tail0 >= 1 && force_tail <= s_max &&
-        tail0 * force_tail <= pairs) {
+    const bool tail_forced = force_split < 1 && force_tail >= 2 && W0 >= 1 && tail0 >= 1 && force_tail <= s_max &&
+                             tail0 * force_tail <= pairs;
+    if (tail_forced) {
         const int S = force_tail;
         plan.tiles_a = (int)(W0 * pairs); plan.split_a = 1; plan.split_b = S;
         plan.clusters = pairs;
@@ -638,6 +744,22 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int pairs) {
     plan.num_units = plan.tiles_a * plan.split_a + (plan.num_tiles - plan.tiles_a) * plan.split_b;
     plan.slots = (plan.split_a > 1 ? (long long)plan.tiles_a * plan.split_a : 0) +
                  (plan.split_b > 1 ? (long long)(plan.num_tiles - plan.tiles_a) * plan.split_b : 0);
+    const int force_chain = env_int("EMU_CHAIN", -1);
+    if (force_split < 1 && !tail_forced && force_chain != 0 && T >= pairs && T > 1) {
+        // without a cut tile a chained plan splits the work as whole-tile
+        // waves do, so it is taken only when forced
+        ChainPlan c;
+        if (chain_plan(T, KS, pairs, force_chain == 2, &c) &&
+            (force_chain >= 1 || (c.cuts > 0 && c.cost < plan.cost - 1e-9))) {
+            plan.tiles_a = (int)T; plan.split_a = 1; plan.split_b = 1;
+            plan.chain = 1;
+            plan.clusters = pairs;
+            plan.num_units = c.units;
+            plan.slots = c.cuts > 0 ? pairs - 1 : 0;
+            plan.cost = c.cost;
+            for (int i = 0; i <= pairs; ++i) plan.chain_bound[i] = c.bound[i];
+        }
+    }
     const int per_unit = (KS + plan.split_a - 1) / plan.split_a;
     const int force_pipe = env_int("EMU_PIPE", -1);
     plan.pipe = force_pipe == PIPE_SHORT_K || force_pipe == PIPE_LONG_K ? force_pipe
@@ -836,6 +958,9 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
     p.k_stages = plan.k_stages;
     p.tiles_a = plan.tiles_a; p.split_a = plan.split_a; p.split_b = plan.split_b;
     p.num_units = plan.num_units;
+    p.chain = plan.chain;
+    if (plan.chain)
+        for (int i = 0; i <= plan.clusters; ++i) p.chain_bound[i] = plan.chain_bound[i];
     p.alpha = alpha; p.beta = beta;
     p.c_old = C; p.c = C; p.ldc = ldc;
     p.bias = bias;
@@ -1127,8 +1252,18 @@ emu_status_t emu_plan_query(int64_t M, int64_t N, int64_t K, int pairs, int64_t*
     const Plan p = make_plan(M, N, K, pairs);
     const int64_t v[EMU_PLAN_FIELDS] = {p.pipe, p.tn, p.tiles_m, p.tiles_n, p.k_stages, p.tiles_a,
                                         p.split_a, p.split_b, p.num_units, p.clusters, p.slots,
-                                        (int64_t)(p.cost * 100.0 + 0.5)};
+                                        (int64_t)(p.cost * 100.0 + 0.5), p.chain};
     for (int i = 0; i < EMU_PLAN_FIELDS; ++i) out[i] = v[i];
+    return EMU_STATUS_SUCCESS;
+}
+
+emu_status_t emu_plan_bounds(int64_t M, int64_t N, int64_t K, int pairs, int64_t* out, int n) {
+    if (M <= 0 || N <= 0 || K <= 0 || pairs < 1 || !out || n < 1) return EMU_STATUS_INVALID_VALUE;
+    if (M > INT32_MAX - 256 || N > INT32_MAX - 256 || K > INT32_MAX - 256) return EMU_STATUS_NOT_SUPPORTED;
+    const Plan p = make_plan(M, N, K, pairs);
+    if (!p.chain) return EMU_STATUS_NOT_SUPPORTED;
+    if (n < p.clusters + 1) return EMU_STATUS_INVALID_VALUE;
+    for (int i = 0; i <= p.clusters; ++i) out[i] = p.chain_bound[i];
     return EMU_STATUS_SUCCESS;
 }
 
@@ -1147,7 +1282,7 @@ emu_status_t emu_dispatch_query(emu_mode_t mode, int64_t M, int64_t N, int64_t K
     return EMU_STATUS_SUCCESS;
 }
 
-int emu_version(void) { return 100; }
+int emu_version(void) { return 200; }
 
 }  // extern "C"
 
@@ -1246,6 +1381,9 @@ emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, 
     p.k_stages = plan.k_stages;
     p.tiles_a = plan.tiles_a; p.split_a = plan.split_a; p.split_b = plan.split_b;
     p.num_units = plan.num_units;
+    p.chain = plan.chain;
+    if (plan.chain)
+        for (int i = 0; i <= plan.clusters; ++i) p.chain_bound[i] = plan.chain_bound[i];
     p.alpha = alpha; p.beta = beta;
     p.c_old = C; p.c = C; p.ldc = ldc;
     p.bias = nullptr;

@@ -40,6 +40,16 @@
 // piece index) -- the result does not depend on timing.  The pieces count
 // their arrivals on epoch-tagged counters (one new epoch per launch), so no
 // count left by an earlier launch can be taken for this one's.
+//
+// Chained plans (more tiles than pairs, not a whole number of waves): the
+// tiles' k-stages, taken tile by tile, are cut into one contiguous run per
+// pair of equal length (to one stage), so every pair has the same work.  A
+// run boundary that falls inside a tile cuts it in two pieces on
+// neighbouring pairs: the pair whose run starts there takes the tile's low
+// k-stages first and publishes its running FP32 sum; the pair whose run ends
+// there takes the high k-stages last and starts its running sum from the
+// published one.  The sum over stages is then the same sequence of roundings
+// as in an uncut tile, so chained plans give the unsplit result bit for bit.
 #pragma once
 
 #include <cstdint>
@@ -65,6 +75,7 @@ constexpr int NUM_SPLIT_THREADS = NUM_SPLIT_WARPS * 32;
 constexpr int WARP_EPI0 = 8;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;         // all of TMEM: 512 / TN accumulators of TN columns
+constexpr int kMaxChainPairs = 160;         // CTA pairs a chained plan can use
 constexpr uint32_t EPI_BARRIER = 1;         // named barrier of the 256 epilogue threads
 constexpr uint32_t SPLIT_BARRIER = 2;       // named barrier of the split threads
 
@@ -204,12 +215,18 @@ struct Params {
     // c + pairs, c + 2 pairs, ...
     int tiles_a, split_a, split_b;
     int num_units;
+    // 1: chained plan (every tile whole in the fields above; the pairs'
+    // stage runs decide the units, see walk_of): pair c runs the stages
+    // [chain_bound[c], chain_bound[c + 1]) of the tile-by-tile sequence
+    int chain;
+    long long chain_bound[kMaxChainPairs + 1];
     float alpha, beta;
     const float* c_old;  // read only when beta != 0
     float* c;
     long long ldc;
     const float* bias;   // may be null
-    float* workspace;    // split tiles: S partial tiles of 256 x TN each (thread-major)
+    float* workspace;    // split tiles: S partial tiles of 256 x TN each (thread-major);
+                         // chained plans: one running sum per run boundary (pairs - 1)
     unsigned long long* counters;  // split tiles: 2 per tile (pieces arrived, per CTA half), epoch-tagged
     unsigned long long epoch;      // this launch's epoch on the counters (> 0, new for every launch)
     unsigned long long wait_budget_ns;
@@ -361,12 +378,21 @@ __device__ __forceinline__ void issue_stage_mmas(uint32_t d, uint32_t a_base, ui
     }
 }
 
+// What the epilogue does with a unit's sums besides adding its stages:
+// ROLE_TILE  a whole tile, or a piece of a reduce-scatter split tile;
+// ROLE_HEAD  chained plans: the low k-stages of a cut tile, whose running sum
+//            is published for the pair that finishes the tile;
+// ROLE_TAIL  chained plans: the high k-stages of a cut tile, whose running
+//            sum starts from the published one; stored like a whole tile.
+enum Role : int { ROLE_TILE = 0, ROLE_HEAD = 1, ROLE_TAIL = 2 };
+
 struct Unit {
-    int tile, piece, pieces, kb, ke;
-    long long slot;  // first workspace partial tile of a split tile
+    int tile, piece, pieces, kb, ke, role;
+    long long slot;  // first workspace partial tile of a split tile; chained plans: the running sum's slot
 };
 __device__ __forceinline__ Unit unit_of(const Params& p, int u) {
     Unit w;
+    w.role = ROLE_TILE;
     const int units_a = p.tiles_a * p.split_a;
     const long long slots_a = p.split_a > 1 ? static_cast<long long>(units_a) : 0;
     if (u < units_a) {
@@ -384,6 +410,46 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int u) {
     }
     w.kb = static_cast<int>((static_cast<long long>(w.piece) * p.k_stages) / w.pieces);
     w.ke = static_cast<int>((static_cast<long long>(w.piece + 1) * p.k_stages) / w.pieces);
+    return w;
+}
+
+// The units one CTA pair runs, in order: u = first, first + step, ... < last.
+// Other plans: every unit index c, c + pairs, ...  Chained plans: the pair's
+// run [s, e) of the tile-major stage sequence (tile t's stages are t * KS ..
+// t * KS + KS - 1, taken in DEcreasing k order, so that a run that starts
+// inside a tile holds its low k-stages); the units are the tiles the run
+// touches, in increasing order.  The planner gives every pair a non-empty run
+// that is not strictly inside one tile, so no tile is cut twice.
+struct Walk {
+    int first, last, step;
+    int lo, hi;  // chained plans: the run covers positions [lo, KS) of tile `first`, [0, hi) of tile last - 1
+};
+__device__ __forceinline__ Walk walk_of(const Params& p, int cid, int ncl) {
+    Walk k;
+    if (!p.chain) {
+        k.first = cid; k.last = p.num_units; k.step = ncl; k.lo = 0; k.hi = 0;
+        return k;
+    }
+    const long long s = p.chain_bound[cid], e = p.chain_bound[cid + 1];  // e > s
+    k.first = static_cast<int>(s / p.k_stages);
+    k.last = static_cast<int>((e - 1) / p.k_stages) + 1;
+    k.step = 1;
+    k.lo = static_cast<int>(s - static_cast<long long>(k.first) * p.k_stages);
+    k.hi = static_cast<int>(e - static_cast<long long>(k.last - 1) * p.k_stages);
+    return k;
+}
+__device__ __forceinline__ Unit unit_at(const Params& p, const Walk& k, int cid, int u) {
+    if (!p.chain) return unit_of(p, u);
+    Unit w;
+    const int lo = u == k.first ? k.lo : 0;                 // the run covers positions
+    const int hi = u == k.last - 1 ? k.hi : p.k_stages;     // [lo, hi) of tile u
+    w.tile = u; w.piece = 0; w.pieces = 1;
+    w.kb = p.k_stages - hi;
+    w.ke = p.k_stages - lo;
+    // the boundary between pairs c - 1 and c owns running-sum slot c - 1
+    if (lo > 0) { w.role = ROLE_HEAD; w.slot = cid - 1; }
+    else if (hi < p.k_stages) { w.role = ROLE_TAIL; w.slot = cid; }
+    else { w.role = ROLE_TILE; w.slot = 0; }
     return w;
 }
 
@@ -421,6 +487,9 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bcomp_empty + NB);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+    // this pair's walk (first, last, step, lo, hi), for the epilogue to read
+    // at each unit instead of holding it in registers across the k-loops
+    volatile int* walk_sh = reinterpret_cast<volatile int*>(tmem_slot + 4);
 
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31u;
     const uint32_t rank = cluster_ctarank();
@@ -474,6 +543,10 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         mbar_init(drain, 1);
         for (int s = 0; s < NB; ++s) { mbar_init(&bcomp_full[s], 1); mbar_init(&bcomp_empty[s], 1); }
         *abort_flag = 0;
+        {
+            const Walk wk = walk_of(p, static_cast<int>(cid), static_cast<int>(ncl));
+            walk_sh[0] = wk.first; walk_sh[1] = wk.last; walk_sh[2] = wk.step; walk_sh[3] = wk.lo; walk_sh[4] = wk.hi;
+        }
         fence_mbar_init();
         // Where the first stages come from depends on the parameters alone:
         // it is worked out before waiting for the previous grid, so that the
@@ -482,13 +555,14 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         constexpr int NE = PACKED && NB > NF ? NB : NF;
         int e_m0[NE], e_n0[NE], e_ks[NE], ne = 0;
         {
-            int u = cid, ks = 0, ke = 0, tile = 0;
+            const Walk wk = walk_of(p, static_cast<int>(cid), static_cast<int>(ncl));
+            int u = wk.first, ks = 0, ke = 0, tile = 0;
 #pragma unroll
             for (int i = 0; i < NE; ++i) {
-                while (ks >= ke && u < p.num_units) {
-                    const Unit w = unit_of(p, u);
+                while (ks >= ke && u < wk.last) {
+                    const Unit w = unit_at(p, wk, static_cast<int>(cid), u);
                     tile = w.tile; ks = w.kb; ke = w.ke;
-                    u += ncl;
+                    u += wk.step;
                 }
                 if (ks < ke) {
                     e_m0[i] = (tile / p.tiles_n) * TILE_M + HALF * rank;
@@ -540,6 +614,7 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
     griddep_wait();           // inputs, C, workspace and counters are the previous grids' to finish
     const uint32_t tmem_base = *tmem_slot;
     const uint64_t budget = p.wait_budget_ns;
+    const Walk walk = walk_of(p, static_cast<int>(cid), static_cast<int>(ncl));
 
     if (warp == WARP_PRODUCER) {
         // ------------------------------------------------------ producer ----
@@ -549,8 +624,8 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
             uint32_t ph = 0, issued_mask = 0, issued_parity = 0;
             uint32_t bph = 0, bissued_mask = 0, bissued_parity = 0;
             bool ok = true;
-            for (int u = cid; ok && u < p.num_units; u += ncl) {
-                const Unit w = unit_of(p, u);
+            for (int u = walk.first; ok && u < walk.last; u += walk.step) {
+                const Unit w = unit_at(p, walk, static_cast<int>(cid), u);
                 for (int ks = w.kb; ks < w.ke; ++ks, ++n) {
                     if (n >= early) {  // the first `early` loads went out before the pair sync
                         if (!mbar_wait(&fp32_empty[s], ph ^ 1u, abort_flag, budget, 1)) { ok = false; break; }
@@ -593,8 +668,8 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
             uint32_t ph = 0, bph = 0;
             bool ok = true, issued = false;
             const uint32_t slice_base = smem_u32(slice_ring), bcomp_base = smem_u32(bcomp_ring);
-            for (int u = cid; ok && u < p.num_units; u += ncl) {
-                const Unit w = unit_of(p, u);
+            for (int u = walk.first; ok && u < walk.last; u += walk.step) {
+                const Unit w = unit_at(p, walk, static_cast<int>(cid), u);
                 for (int ks = w.kb; ks < w.ke; ++ks) {
                     if (!mbar_wait(&acc_empty[b], bph ^ 1u, abort_flag, budget, 2)) { ok = false; break; }
                     if (!mbar_wait(&slice_full[s], ph, abort_flag, budget, 2)) { ok = false; break; }
@@ -628,8 +703,8 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         int fs = 0, ss = 0, bs = 0;
         uint32_t fph = 0, sph = 0, bph = 0;
         bool ok = true;
-        for (int u = cid; ok && u < p.num_units; u += ncl) {
-            const Unit w = unit_of(p, u);
+        for (int u = walk.first; ok && u < walk.last; u += walk.step) {
+            const Unit w = unit_at(p, walk, static_cast<int>(cid), u);
             for (int ks = w.kb; ks < w.ke; ++ks) {
                 if (!mbar_wait_warp(&fp32_full[fs], fph, abort_flag, budget, 3)) { ok = false; break; }
                 if (!mbar_wait_warp(&slice_empty[ss], sph ^ 1u, abort_flag, budget, 3)) { ok = false; break; }
@@ -666,11 +741,36 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         int b = 0;
         uint32_t bph = 0;
         bool ok = true;
-        for (int u = cid; ok && u < p.num_units; u += ncl) {
-            const Unit w = unit_of(p, u);
+        for (int u = walk_sh[0]; ok && u < walk_sh[1]; u += walk_sh[2]) {
+            Walk wk;
+            wk.first = walk_sh[0]; wk.last = walk_sh[1]; wk.step = walk_sh[2]; wk.lo = walk_sh[3]; wk.hi = walk_sh[4];
+            const Unit w = unit_at(p, wk, static_cast<int>(cid), u);
+            // a chained tile's running sum: one 256 x TN slot per run boundary,
+            // thread-major like the split-K partials below (worked out where it
+            // is used, so that it holds no registers during the k-loop)
+            auto chain_sum = [&](long long slot) {
+                return p.workspace + static_cast<size_t>(slot) * (static_cast<size_t>(TILE_M) * TN) +
+                       (static_cast<size_t>(rank) * NUM_EPI_WARPS + e) * (32u * ACC) + lane * 4u;
+            };
             float acc[ACC];
+            if (w.role == ROLE_TAIL) {
+                // Start from the running sum of the tile's low k-stages, which
+                // the next pair publishes at the start of its run.  Each warp
+                // waits for it on its own; all its loads go out at once,
+                // straight into the sums' registers, while the tensor cores
+                // work on this unit's first stages.
+                const unsigned long long* ctr = p.counters + static_cast<size_t>(w.tile) * 2 + rank;
+                if (!warp_wait_epoch(ctr, p.epoch, 1u, abort_flag, budget, 7)) { ok = false; break; }
+                const float* head = chain_sum(w.slot);
 #pragma unroll
-            for (int i = 0; i < ACC; ++i) acc[i] = 0.0f;
+                for (int j = 0; j < ACC / 4; ++j) {
+                    const float4 x = __ldcg(reinterpret_cast<const float4*>(head + j * 128));
+                    acc[4 * j] = x.x; acc[4 * j + 1] = x.y; acc[4 * j + 2] = x.z; acc[4 * j + 3] = x.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < ACC; ++i) acc[i] = 0.0f;
+            }
             for (int ks = w.kb; ks < w.ke; ++ks) {
                 if (!mbar_wait_warp(&acc_full[b], bph, abort_flag, budget, 4)) { ok = false; break; }
                 tc_fence_after();
@@ -696,6 +796,19 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                 if (++b == NACC) { b = 0; bph ^= 1u; }
             }
             if (!ok) break;
+            if (w.role == ROLE_HEAD) {
+                // publish this tile's running sum for the pair that runs its
+                // high k-stages; nothing is stored to C here
+                float* head = chain_sum(w.slot);
+#pragma unroll
+                for (int j = 0; j < ACC / 4; ++j)
+                    __stcg(reinterpret_cast<float4*>(head + j * 128),
+                           make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]));
+                __threadfence();
+                named_bar_sync(EPI_BARRIER, NUM_EPI_WARPS * 32);
+                if (e == 0 && lane == 0) epoch_arrive(p.counters + static_cast<size_t>(w.tile) * 2 + rank, p.epoch);
+                continue;
+            }
             // Split tiles: a reduce-scatter over the tile's S pieces, which all
             // run at the same time (the plan keeps a tile's pieces in one wave
             // of units).  Chunk q = 4e + c (32 columns of

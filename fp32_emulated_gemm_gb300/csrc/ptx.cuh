@@ -173,6 +173,46 @@ __device__ __forceinline__ bool wait_epoch_count(const unsigned long long* ctr, 
     }
 }
 
+// Warp-collective: whether this launch's `target` arrivals are on `ctr`
+// now.  Every lane reads the counter with acquire semantics, so that its own
+// later loads see what the arriving CTAs released; no lane waits.
+__device__ __forceinline__ bool warp_published(const unsigned long long* ctr, unsigned long long epoch,
+                                               unsigned target) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(ctr) : "memory");
+    return __all_sync(0xFFFFFFFFu, (v >> 8) == epoch && (v & 0xFFu) >= target);
+}
+
+// Warp-collective wait for `target` arrivals of `epoch` on `ctr`: every lane
+// polls with acquire semantics until all see them; lane 0 keeps the time
+// budget like the other waits.  False after a timeout or an abort.
+__device__ __forceinline__ bool warp_wait_epoch(const unsigned long long* ctr, unsigned long long epoch,
+                                                unsigned target, volatile int* abort, uint64_t budget_ns,
+                                                unsigned role) {
+    const uint32_t lane = threadIdx.x & 31u;
+    uint64_t t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (warp_published(ctr, epoch, target)) return true;
+        if ((i & 7u) == 7u) {
+            int give_up = 0;
+            if (lane == 0) {
+                const uint64_t now = globaltimer_ns();
+                if (*abort) {
+                    give_up = 1;
+                } else if (t0 == 0) {
+                    t0 = now;
+                } else if (now - t0 > budget_ns) {
+                    atomicOr(&g_error_flag, ERR_TIMEOUT | (role << 8));
+                    *abort = 1;
+                    give_up = 1;
+                }
+            }
+            if (__shfl_sync(0xFFFFFFFFu, give_up, 0)) return false;
+        }
+        __nanosleep(64);
+    }
+}
+
 // Warp-collective form: every lane polls, and the warp stops together, so
 // that the .sync.aligned instructions that follow see a converged warp.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort,

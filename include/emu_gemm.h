@@ -310,7 +310,7 @@ emu_status_t emu_debug_fail_allocations(int n);
  * emu_plan_query -- diagnostic, host only (no GPU, no CUDA call): the launch
  * plan emu_sgemm would use for an M x N x K product on a device with `pairs`
  * co-resident CTA pairs (76 on a GB300), honouring the EMU_SPLIT_K,
- * EMU_SPLIT_TAIL and EMU_PIPE overrides.  Writes EMU_PLAN_FIELDS values to out[0..]:
+ * EMU_SPLIT_TAIL, EMU_CHAIN and EMU_PIPE overrides.  Writes EMU_PLAN_FIELDS values to out[0..]:
  *   0 pipeline shape (0 short-k, 1 long-k)   1 tile width (256)
  *   2 tiles along M (256 rows each)          3 tiles along N
  *   4 k-stages (32 each)                     5 tiles processed first (tiles_a)
@@ -320,13 +320,31 @@ emu_status_t emu_debug_fail_allocations(int n);
  *  11 predicted time in hundredths of a pipeline stage (waves of work
  *     units, each its k-stages plus the output stores, plus the split-K
  *     reduction), the figure the plan minimises
+ *  12 chained plan (1) or not (0)
  * Work unit u of the first group is piece u % split_a of tile u / split_a;
  * the remaining tiles follow, split_b units each; pair c runs units c,
- * c + pairs launched, ...  INVALID_VALUE for non-positive sizes, pairs < 1,
- * a NULL `out` or n < EMU_PLAN_FIELDS.
+ * c + pairs launched, ...  A chained plan (at least as many tiles as pairs;
+ * fields 5-7 then read all tiles, 1, 1) instead gives pair c the stages
+ * [b_c, b_c+1) of the U = tiles x k-stages stages taken tile by tile, each
+ * tile's in decreasing k order (emu_plan_bounds gives b_0 = 0 < b_1 < ... <
+ * b_P = U, P = pairs launched; each b_c lies within 2 stages of c U / P).
+ * A tile that a run boundary cuts is split in two: the pair whose run starts
+ * in it runs its low k-stages first and publishes the running FP32 sum (in
+ * the workspace, one 256 x 256 slot per boundary); the pair whose run ends in
+ * it runs the high k-stages last, starting from that sum, and stores the
+ * tile.  The result is bit for bit that of the uncut tile.  INVALID_VALUE for
+ * non-positive sizes, pairs < 1, a NULL `out` or n < EMU_PLAN_FIELDS.
  */
-#define EMU_PLAN_FIELDS 12
+#define EMU_PLAN_FIELDS 13
 emu_status_t emu_plan_query(int64_t M, int64_t N, int64_t K, int pairs, int64_t *out, int n);
+
+/*
+ * emu_plan_bounds -- diagnostic, host only: the run bounds b_0..b_P of the
+ * chained plan emu_plan_query describes (P + 1 values to out[0..]).
+ * NOT_SUPPORTED when that plan is not chained; INVALID_VALUE as for
+ * emu_plan_query, or when n < P + 1.
+ */
+emu_status_t emu_plan_bounds(int64_t M, int64_t N, int64_t K, int pairs, int64_t *out, int n);
 
 /*
  * Strategy.  Blog: "BF16x9 on Blackwell GPUs" (Fig. 4) compares two: the

@@ -93,11 +93,13 @@ def test_multiwave_split_plan_matches_tensor_core_model(mode, monkeypatch):
 
 
 @pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
-def test_hybrid_plan_matches_tensor_core_model(mode):
-    """The library's own plan for the PET-small forward pass: whole tiles in
-    the first wave, the tail tiles split.  Rows of whole tiles follow the
-    unsplit model, rows of tail tiles the split one."""
+def test_hybrid_plan_matches_tensor_core_model(mode, monkeypatch):
+    """The hybrid plan for the PET-small forward pass (the library chains
+    this product by default; EMU_CHAIN=0 gives the plan it would take
+    otherwise): whole tiles in the first wave, the tail tiles split.  Rows of
+    whole tiles follow the unsplit model, rows of tail tiles the split one."""
     import fp32_emulated_gemm_gb300 as emu
+    monkeypatch.setenv("EMU_CHAIN", "0")
     s = W.PET_SMALL
     plan = emu.emu_plan_query(s.M, s.N, s.K, 76)
     assert plan["split_a"] == 1 and plan["split_b"] > 1 and plan["tiles_a"] % plan["tiles_n"] == 0

@@ -63,6 +63,33 @@ def test_split_launch_after_a_split_timeout_is_correct(mode, pieces, monkeypatch
     _gpu.compare(mode, C, p, label=f"after split timeout, {pieces} pieces")
 
 
+@pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
+def test_chained_launch_after_a_timeout_is_correct(mode, monkeypatch):
+    """A chained plan (80 tiles on 76 pairs) waits for one arrival on a cut
+    tile's counter before it reads the published running sum.  After a
+    chained launch on other inputs and a timed-out wait that leaves one
+    arrival on every counter, the next chained launch on the same stream must
+    give the bits of the unsplit plan."""
+    import fp32_emulated_gemm_gb300 as emu
+    M, N, K = 2000, 2500, 200
+    monkeypatch.setenv("EMU_CHAIN", "1")
+    assert emu.emu_plan_query(M, N, K, 76)["chain"] == 1
+    A, B = _problem(43, M, N, K)
+    A_other, B_other = _problem(44, M, N, K)
+    Ad, Bd = _gpu.to_dev(A), _gpu.to_dev(B)
+    emu.sgemm(_gpu.to_dev(A_other), _gpu.to_dev(B_other), mode=mode)  # other running sums left behind
+    assert emu.emu_stream_check() == 0
+    emu.emu_selftest_split_timeout(2_000_000, 8 * 10)
+    assert emu.emu_stream_check() == DEVICE_TIMEOUT
+    C = emu.sgemm(Ad, Bd, mode=mode).cpu().numpy()
+    assert emu.emu_stream_check() == 0
+    monkeypatch.setenv("EMU_CHAIN", "0")
+    monkeypatch.setenv("EMU_SPLIT_K", "1")
+    _same_bits(C, emu.sgemm(Ad, Bd, mode=mode).cpu().numpy())
+    rows = np.arange(0, M, 53)
+    _gpu.compare(mode, C, oracle.Problem(A, B), rows, label="chained, after a timeout")
+
+
 def test_shutdown_releases_buffers_and_later_calls_allocate_again(monkeypatch):
     """emu_shutdown frees every cached workspace and pre-split buffer; the
     next split call (and a TF32x3 call that pre-splits op(B)) allocates

@@ -41,11 +41,19 @@ def _stream():
 
 
 @pytest.mark.parametrize("mode", ["bf16x9", "tf32x3"])
-@pytest.mark.parametrize("case", ["split_k", "single_piece"])
+@pytest.mark.parametrize("case", ["split_k", "single_piece", "chained"])
 def test_noalloc_matches_emu_sgemm_on_two_calls(mode, case):
     import torch
     import fp32_emulated_gemm_gb300 as emu
-    if case == "split_k":
+    if case == "chained":
+        # 96 tiles of 8 k-stages on 76 pairs: a chained plan, whose cut tiles
+        # pass their running sums through the scratch array
+        M, N, K = 6144, 1024, 256
+        assert emu.emu_plan_query(M, N, K, 76)["chain"] == 1
+        rng = np.random.default_rng(23)
+        A = rng.standard_normal((M, K)).astype(np.float32)
+        B = rng.standard_normal((K, N)).astype(np.float32)
+    elif case == "split_k":
         # input gradient of the PET-small layer: 24 tiles, K split into 3 pieces
         s = W.PET_SMALL
         _, Wt, _, dY = W.linear_inputs(s, W.CONFIG_ID["pet_small"])
