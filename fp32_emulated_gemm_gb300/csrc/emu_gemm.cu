@@ -582,6 +582,7 @@ int env_int(const char* name, int dflt) {
 // twice).
 constexpr double kChainDrainStages = 2.0, kChainShortTailStages = 2.0;
 constexpr int kChainSlack = 2;  // each bound within this many stages of the even cut c U / pairs
+static_assert(kChainSlack <= 127, "bounds travel to the kernel as signed bytes (Params::chain_delta)");
 double chain_run_cost(long long s, long long e, int KS) {
     if (e <= s) return -1.0;
     const long long t0 = s / KS, t1 = (e - 1) / KS;
@@ -959,8 +960,13 @@ emu_status_t run_gemm(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, int64_t 
     p.tiles_a = plan.tiles_a; p.split_a = plan.split_a; p.split_b = plan.split_b;
     p.num_units = plan.num_units;
     p.chain = plan.chain;
-    if (plan.chain)
-        for (int i = 0; i <= plan.clusters; ++i) p.chain_bound[i] = plan.chain_bound[i];
+    if (plan.chain) {
+        const long long U = (long long)plan.num_tiles * plan.k_stages;
+        p.chain_q = U / plan.clusters;
+        p.chain_r = (int)(U % plan.clusters);
+        for (int i = 0; i <= plan.clusters; ++i)
+            p.chain_delta[i] = (signed char)(plan.chain_bound[i] - (long long)i * U / plan.clusters);
+    }
     p.alpha = alpha; p.beta = beta;
     p.c_old = C; p.c = C; p.ldc = ldc;
     p.bias = bias;
@@ -1382,8 +1388,13 @@ emu_status_t run_gemm_noalloc(emu_mode_t mode, bool a_mn, bool b_mn, int64_t M, 
     p.tiles_a = plan.tiles_a; p.split_a = plan.split_a; p.split_b = plan.split_b;
     p.num_units = plan.num_units;
     p.chain = plan.chain;
-    if (plan.chain)
-        for (int i = 0; i <= plan.clusters; ++i) p.chain_bound[i] = plan.chain_bound[i];
+    if (plan.chain) {
+        const long long U = (long long)plan.num_tiles * plan.k_stages;
+        p.chain_q = U / plan.clusters;
+        p.chain_r = (int)(U % plan.clusters);
+        for (int i = 0; i <= plan.clusters; ++i)
+            p.chain_delta[i] = (signed char)(plan.chain_bound[i] - (long long)i * U / plan.clusters);
+    }
     p.alpha = alpha; p.beta = beta;
     p.c_old = C; p.c = C; p.ldc = ldc;
     p.bias = nullptr;

@@ -217,9 +217,14 @@ struct Params {
     int num_units;
     // 1: chained plan (every tile whole in the fields above; the pairs'
     // stage runs decide the units, see walk_of): pair c runs the stages
-    // [chain_bound[c], chain_bound[c + 1]) of the tile-by-tile sequence
+    // [b_c, b_c+1) of the tile-by-tile sequence, b_c = c U / pairs +
+    // chain_delta[c] (U = num_tiles * k_stages; |chain_delta| <= 2), with
+    // c U / pairs = c chain_q + (c chain_r) / pairs (U = chain_q pairs +
+    // chain_r), which needs no 64-bit division
     int chain;
-    long long chain_bound[kMaxChainPairs + 1];
+    int chain_r;
+    long long chain_q;
+    signed char chain_delta[kMaxChainPairs + 1];
     float alpha, beta;
     const float* c_old;  // read only when beta != 0
     float* c;
@@ -430,7 +435,8 @@ __device__ __forceinline__ Walk walk_of(const Params& p, int cid, int ncl) {
         k.first = cid; k.last = p.num_units; k.step = ncl; k.lo = 0; k.hi = 0;
         return k;
     }
-    const long long s = p.chain_bound[cid], e = p.chain_bound[cid + 1];  // e > s
+    const long long s = cid * p.chain_q + (cid * p.chain_r) / ncl + p.chain_delta[cid];
+    const long long e = (cid + 1) * p.chain_q + ((cid + 1) * p.chain_r) / ncl + p.chain_delta[cid + 1];  // e > s
     k.first = static_cast<int>(s / p.k_stages);
     k.last = static_cast<int>((e - 1) / p.k_stages) + 1;
     k.step = 1;
@@ -543,10 +549,9 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         mbar_init(drain, 1);
         for (int s = 0; s < NB; ++s) { mbar_init(&bcomp_full[s], 1); mbar_init(&bcomp_empty[s], 1); }
         *abort_flag = 0;
-        {
-            const Walk wk = walk_of(p, static_cast<int>(cid), static_cast<int>(ncl));
-            walk_sh[0] = wk.first; walk_sh[1] = wk.last; walk_sh[2] = wk.step; walk_sh[3] = wk.lo; walk_sh[4] = wk.hi;
-        }
+        // this pair's walk, worked out once for all roles
+        const Walk wk = walk_of(p, static_cast<int>(cid), static_cast<int>(ncl));
+        walk_sh[0] = wk.first; walk_sh[1] = wk.last; walk_sh[2] = wk.step; walk_sh[3] = wk.lo; walk_sh[4] = wk.hi;
         fence_mbar_init();
         // Where the first stages come from depends on the parameters alone:
         // it is worked out before waiting for the previous grid, so that the
@@ -555,41 +560,39 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
         constexpr int NE = PACKED && NB > NF ? NB : NF;
         int e_m0[NE], e_n0[NE], e_ks[NE], ne = 0;
         {
-            const Walk wk = walk_of(p, static_cast<int>(cid), static_cast<int>(ncl));
-            int u = wk.first, ks = 0, ke = 0, tile = 0;
+            int u = wk.first, ks = 0, ke = 0, m0 = 0, n0 = 0;
 #pragma unroll
             for (int i = 0; i < NE; ++i) {
                 while (ks >= ke && u < wk.last) {
                     const Unit w = unit_at(p, wk, static_cast<int>(cid), u);
-                    tile = w.tile; ks = w.kb; ke = w.ke;
+                    const int tm = w.tile / p.tiles_n;
+                    m0 = tm * TILE_M + HALF * rank;
+                    n0 = (w.tile - tm * p.tiles_n) * TN + BH * rank;
+                    ks = w.kb; ke = w.ke;
                     u += wk.step;
                 }
                 if (ks < ke) {
-                    e_m0[i] = (tile / p.tiles_n) * TILE_M + HALF * rank;
-                    e_n0[i] = (tile % p.tiles_n) * TN + BH * rank;
+                    e_m0[i] = m0;
+                    e_n0[i] = n0;
                     e_ks[i] = ks++;
                     ne = i + 1;
                 }
             }
         }
-        // the first stages' operands are prefetched into L2 while the
-        // previous grid finishes (L2 is coherent, so nothing stale is read)
-#pragma unroll
-        for (int i = 0; i < NE; ++i) {
-            if (i < ne) {
-                const int k0 = e_ks[i] * BK;
-                if (i < NF) {
-                    if (!p.a_mn_major) tma_prefetch_l2_2d(&p.tmA, k0, e_m0[i]);
-                    else for (int j = 0; j < HALF / 32; ++j) tma_prefetch_l2_2d(&p.tmA, e_m0[i] + 32 * j, k0);
-                    if constexpr (!PACKED) {
-                        if (!p.b_mn_major) tma_prefetch_l2_2d(&p.tmB, k0, e_n0[i]);
-                        else for (int j = 0; j < BH / 32; ++j) tma_prefetch_l2_2d(&p.tmB, e_n0[i] + 32 * j, k0);
-                    }
-                }
-                if constexpr (PACKED) {
-                    if (i < NB)
-                        for (int c = 0; c < C::NCOMP; ++c) tma_prefetch_l2_3d(&p.tmB, k0, e_n0[i], c);
-                }
+        // the first stage's operands are prefetched into L2 while the
+        // previous grid finishes (L2 is coherent, so nothing stale is read);
+        // the later stages' loads go out right after the wait anyway, and
+        // each prefetch costs this thread issue time when nothing is waited
+        // for
+        if (ne > 0) {
+            const int k0 = e_ks[0] * BK;
+            if (!p.a_mn_major) tma_prefetch_l2_2d(&p.tmA, k0, e_m0[0]);
+            else for (int j = 0; j < HALF / 32; ++j) tma_prefetch_l2_2d(&p.tmA, e_m0[0] + 32 * j, k0);
+            if constexpr (!PACKED) {
+                if (!p.b_mn_major) tma_prefetch_l2_2d(&p.tmB, k0, e_n0[0]);
+                else for (int j = 0; j < BH / 32; ++j) tma_prefetch_l2_2d(&p.tmB, e_n0[0] + 32 * j, k0);
+            } else {
+                for (int c = 0; c < C::NCOMP; ++c) tma_prefetch_l2_3d(&p.tmB, k0, e_n0[0], c);
             }
         }
         griddep_wait();
@@ -614,7 +617,8 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
     griddep_wait();           // inputs, C, workspace and counters are the previous grids' to finish
     const uint32_t tmem_base = *tmem_slot;
     const uint64_t budget = p.wait_budget_ns;
-    const Walk walk = walk_of(p, static_cast<int>(cid), static_cast<int>(ncl));
+    Walk walk;  // (thread 0's, from shared memory)
+    walk.first = walk_sh[0]; walk.last = walk_sh[1]; walk.step = walk_sh[2]; walk.lo = walk_sh[3]; walk.hi = walk_sh[4];
 
     if (warp == WARP_PRODUCER) {
         // ------------------------------------------------------ producer ----
@@ -753,7 +757,7 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                        (static_cast<size_t>(rank) * NUM_EPI_WARPS + e) * (32u * ACC) + lane * 4u;
             };
             float acc[ACC];
-            if (w.role == ROLE_TAIL) {
+            if (!STAGED && w.role == ROLE_TAIL) {
                 // Start from the running sum of the tile's low k-stages, which
                 // the next pair publishes at the start of its run.  Each warp
                 // waits for it on its own; all its loads go out at once,
@@ -796,7 +800,7 @@ emu_gemm_kernel(const __grid_constant__ Params p) {
                 if (++b == NACC) { b = 0; bph ^= 1u; }
             }
             if (!ok) break;
-            if (w.role == ROLE_HEAD) {
+            if (!STAGED && w.role == ROLE_HEAD) {
                 // publish this tile's running sum for the pair that runs its
                 // high k-stages; nothing is stored to C here
                 float* head = chain_sum(w.slot);
