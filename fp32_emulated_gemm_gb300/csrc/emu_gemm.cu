@@ -572,15 +572,18 @@ int env_int(const char* name, int dflt) {
 
 // Chained plans (T >= pairs tiles of KS stages; the U = T KS stages taken
 // tile by tile, pair c runs [bound[c], bound[c + 1])).  What a pair's run
-// costs, in pipeline stages (measured on GB300 with globaltimer stamps of the
-// PET-small forward pass): its stages; about 2 more for every unit before the
-// last, whose output stores (or published running sum) the next unit's first
-// two stages hide only in part; about 2 more when the last unit is a short
-// tail (2 stages or fewer) right after a whole tile, because the tail's
-// starting-sum loads queue behind that tile's stores.  Every run covers at
-// least one tile end or start (a run strictly inside one tile would cut it
-// twice).
-constexpr double kChainDrainStages = 2.0, kChainShortTailStages = 2.0;
+// costs, in pipeline stages: its stages, plus, at each step from one unit to
+// the next, the part of the first unit's output phase (128 KB of stores per
+// CTA, or its published running sum) that the next unit's first two stages
+// do not hide.  Measured on GB300 with globaltimer stamps of the PET-small
+// forward pass (pairs of 8-11 stages; the end of each pair against a pair
+// that runs one whole tile): head -> whole tile 1.1 stages, head -> tail
+// 1.6, whole tile -> tail 4 (the tail's starting-sum loads queue behind the
+// tile's stores in the SM's memory pipeline; a head's publish ends with a
+// fence, so a tail after a head loads at once), whole tile -> whole tile
+// about 2.  Every run covers at least one tile end or start (a run strictly
+// inside one tile would cut it twice).
+constexpr double kChainHeadToTile = 1.1, kChainHeadToTail = 1.6, kChainTileToTile = 2.0, kChainTileToTail = 4.0;
 constexpr int kChainSlack = 2;  // each bound within this many stages of the even cut c U / pairs
 static_assert(kChainSlack <= 127, "bounds travel to the kernel as signed bytes (Params::chain_delta)");
 double chain_run_cost(long long s, long long e, int KS) {
@@ -588,9 +591,12 @@ double chain_run_cost(long long s, long long e, int KS) {
     const long long t0 = s / KS, t1 = (e - 1) / KS;
     const long long units = t1 - t0 + 1, lo = s - t0 * KS, hi = e - t1 * KS;
     if (units == 1 && lo > 0 && hi < KS) return -1.0;
-    double c = (double)(e - s) + kChainDrainStages * (double)(units - 1);
-    if (hi < KS && units >= 2 && (units >= 3 || lo == 0) && hi <= 2) c += kChainShortTailStages;
-    return c;
+    double c = (double)(e - s);
+    if (units == 1) return c;
+    const bool head = lo > 0, tail = hi < KS;
+    if (units == 2) return c + (head ? (tail ? kChainHeadToTail : kChainHeadToTile) : (tail ? kChainTileToTail : kChainTileToTile));
+    return c + (head ? kChainHeadToTile : kChainTileToTile) + kChainTileToTile * (double)(units - 3) +
+           (tail ? kChainTileToTail : kChainTileToTile);
 }
 
 struct ChainPlan {

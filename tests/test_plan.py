@@ -43,18 +43,15 @@ def _chain_runs(plan, bounds):
 
 def _run_cost(units, KS):
     """The planner's cost of one pair's run, in pipeline stages: its stages,
-    2 per unit before the last, 2 more for a last unit of at most 2 stages
-    that is a tail (the high k-stages of a cut tile) right after a whole
-    tile."""
-    n = sum(ke - kb for (_, kb, ke) in units)
-    c = n + 2.0 * (len(units) - 1)
-    last_t, last_kb, last_ke = units[-1]
-    tail = last_ke == KS and last_kb > 0
-    if len(units) >= 2 and tail and last_ke - last_kb <= 2:
-        prev_t, prev_kb, prev_ke = units[-2]
-        if (prev_kb, prev_ke) == (0, KS):
-            c += 2.0
-    return c
+    plus a cost for each step from one unit to the next by the kinds of the
+    two units (head = the low k-stages of a cut tile, tail = its high ones,
+    whole = an uncut tile): head -> whole 1.1, head -> tail 1.6,
+    whole -> whole 2, whole -> tail 4."""
+    def kind(kb, ke):
+        return "head" if kb == 0 and ke < KS else ("tail" if ke == KS and kb > 0 else "whole")
+    step = {("head", "whole"): 1.1, ("head", "tail"): 1.6, ("whole", "whole"): 2.0, ("whole", "tail"): 4.0}
+    kinds = [kind(kb, ke) for (_, kb, ke) in units]
+    return sum(ke - kb for (_, kb, ke) in units) + sum(step[(a, b)] for a, b in zip(kinds, kinds[1:]))
 
 
 def _check_chain(M, N, K, pairs, plan):
