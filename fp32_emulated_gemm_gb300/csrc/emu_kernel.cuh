@@ -413,8 +413,10 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int u) {
         w.piece = v - t * p.split_b;
         w.slot = slots_a + static_cast<long long>(t) * p.split_b;
     }
-    w.kb = static_cast<int>((static_cast<long long>(w.piece) * p.k_stages) / w.pieces);
-    w.ke = static_cast<int>((static_cast<long long>(w.piece + 1) * p.k_stages) / w.pieces);
+    // (piece + 1) * k_stages < 32 * 2^26 fits 32 unsigned bits: no 64-bit division
+    const uint32_t ks = static_cast<uint32_t>(p.k_stages), np = static_cast<uint32_t>(w.pieces);
+    w.kb = static_cast<int>(static_cast<uint32_t>(w.piece) * ks / np);
+    w.ke = static_cast<int>(static_cast<uint32_t>(w.piece + 1) * ks / np);
     return w;
 }
 
