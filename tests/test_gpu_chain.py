@@ -124,3 +124,36 @@ def test_chained_input_gradient_shape(mode, monkeypatch):
     p = oracle.Problem(dY, Wt)
     _same_bits(dX[rows], oracle.gemm_tc(p, mode=mode, rows=rows, pieces=1), "chained vs tensor-core model")
     _gpu.compare(mode, dX, p, rows, label="chained input gradient")
+
+
+@pytest.mark.parametrize("case", range(6))
+def test_random_chained_shapes_give_the_unsplit_bits(case, monkeypatch):
+    """Seeded random shapes with at least as many tiles as CTA pairs (so the
+    plan can chain), random layouts, alpha, beta and C_old, and both bound
+    choices: every element equal to the unsplit plan's, sampled rows equal to
+    the tensor-core model's."""
+    import fp32_emulated_gemm_gb300 as emu
+    rng = np.random.default_rng(3000 + case)
+    mode = ["bf16x9", "tf32x3", "bf16x6", "tf32x1"][case % 4]
+    while True:
+        M, N = int(rng.integers(1500, 6000)), int(rng.integers(1500, 4500))
+        K = int(rng.integers(33, 700))
+        if -(-M // 256) * -(-N // 256) >= PAIRS:
+            break
+    tA, tB = bool(rng.integers(0, 2)), bool(rng.integers(0, 2))
+    alpha, beta = float(rng.choice([1.0, 0.5, -1.25])), float(rng.choice([0.0, 1.0, -0.75]))
+    A = rng.standard_normal((K, M) if tA else (M, K)).astype(np.float32)
+    B = rng.standard_normal((N, K) if tB else (K, N)).astype(np.float32)
+    Cold = rng.standard_normal((M, N)).astype(np.float32)
+    kw = dict(transA=tA, transB=tB, alpha=alpha, beta=beta, C_old=Cold)
+    chain = "1" if case % 2 == 0 else "2"
+    monkeypatch.setenv("EMU_CHAIN", chain)
+    plan = emu.emu_plan_query(M, N, K, PAIRS)
+    assert plan["chain"] == 1, plan
+    C = _gpu.gpu_sgemm(mode, A, B, **kw)
+    assert emu.emu_stream_check() == 0
+    _unsplit(monkeypatch)
+    _same_bits(C, _gpu.gpu_sgemm(mode, A, B, **kw), f"chained vs unsplit, {mode} M={M} N={N} K={K} tA={tA} tB={tB}")
+    rows = np.unique(rng.integers(0, M, size=12)).astype(np.int64)
+    p = oracle.Problem(A, B, transA=tA, transB=tB, alpha=alpha, beta=beta, C_old=Cold)
+    _same_bits(C[rows], oracle.gemm_tc(p, mode=mode, rows=rows, pieces=1), "chained vs tensor-core model")
