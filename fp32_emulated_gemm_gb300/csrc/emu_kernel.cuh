@@ -439,8 +439,14 @@ __device__ __forceinline__ Walk walk_of(const Params& p, int cid, int ncl) {
     }
     const long long s = cid * p.chain_q + (cid * p.chain_r) / ncl + p.chain_delta[cid];
     const long long e = (cid + 1) * p.chain_q + ((cid + 1) * p.chain_r) / ncl + p.chain_delta[cid + 1];  // e > s
-    k.first = static_cast<int>(s / p.k_stages);
-    k.last = static_cast<int>((e - 1) / p.k_stages) + 1;
+    if (e <= 0x7FFFFFFFll) {  // the usual case: 32-bit divisions (a 64-bit one is a long software routine)
+        const uint32_t ks = static_cast<uint32_t>(p.k_stages);
+        k.first = static_cast<int>(static_cast<uint32_t>(s) / ks);
+        k.last = static_cast<int>(static_cast<uint32_t>(e - 1) / ks) + 1;
+    } else {
+        k.first = static_cast<int>(s / p.k_stages);
+        k.last = static_cast<int>((e - 1) / p.k_stages) + 1;
+    }
     k.step = 1;
     k.lo = static_cast<int>(s - static_cast<long long>(k.first) * p.k_stages);
     k.hi = static_cast<int>(e - static_cast<long long>(k.last - 1) * p.k_stages);
