@@ -231,15 +231,17 @@ emu_status_t emu_split_dump(emu_mode_t mode, int64_t R, int64_t Kc, const float 
  *
  * Same arguments, same plan and same kernel as emu_sgemm (results are the
  * same bits).  The only device memory emu_sgemm may allocate is the split-K
- * scratch (partial tiles and counters for problems with few tiles); here it
- * lives in a fixed 64 MiB device array inside the library instead.  The
- * array is reserved on every GPU that loads the library and kept until the
- * process exits.
+ * scratch (partial tiles and counters for problems with few tiles, running
+ * sums and counters for chained plans); here it lives in a fixed 64 MiB
+ * device array inside the library instead.  The array is reserved on every
+ * GPU that loads the library and kept until the process exits.
  *   - Size limit: a plan that splits some tiles into S pieces needs
- *     (split tiles) * S * 256 KiB (+ 16 bytes per tile, tiles = ceil(M/256) *
- *     ceil(N/256)); if that exceeds 64 MiB the call returns
- *     EMU_STATUS_NOT_SUPPORTED and enqueues nothing.  Plans without a split
- *     use no scratch and are never rejected for size.
+ *     (split tiles) * S * 256 KiB, a chained plan that cuts tiles
+ *     (pairs - 1) * 256 KiB (19 MiB with 76 pairs), each + 16 bytes per
+ *     tile (tiles = ceil(M/256) * ceil(N/256)); if that exceeds 64 MiB the
+ *     call returns EMU_STATUS_NOT_SUPPORTED and enqueues nothing.  Plans
+ *     without a split or a cut use no scratch and are never rejected for
+ *     size.
  *   - Allocation: none (no cudaMalloc/cudaFree, no allocating library
  *     routine).  The call enqueues one cudaMemsetAsync of the counters (the
  *     array keeps the previous call's contents, and the counters are cleared
