@@ -578,9 +578,9 @@ int env_int(const char* name, int dflt) {
 // do not hide.  Measured on GB300 with globaltimer stamps of the PET-small
 // forward pass (pairs of 8-11 stages; the end of each pair against a pair
 // that runs one whole tile): head -> whole tile 1.1 stages, head -> tail
-// 1.6, whole tile -> tail 4 (the tail's starting-sum loads queue behind the
-// tile's stores in the SM's memory pipeline; a head's publish ends with a
-// fence, so a tail after a head loads at once), whole tile -> whole tile
+// 1.6, whole tile -> tail 4 (the short tails that follow a whole tile give
+// the tensor cores too little work to cover the tile's output phase, and
+// their starting-sum loads only go out after it), whole tile -> whole tile
 // about 2.  Every run covers at least one tile end or start (a run strictly
 // inside one tile would cut it twice).
 constexpr double kChainHeadToTile = 1.1, kChainHeadToTail = 1.6, kChainTileToTile = 2.0, kChainTileToTail = 4.0;
